@@ -1,0 +1,85 @@
+/*
+ * attn_oracle.h -- slow, plain fp64 CPU oracle for exact scaled-dot-product
+ * attention forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this library: only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or helper with
+ * the CUDA library.
+ *
+ * What it computes (the plain definition; the tiled GPU method reaches the
+ * same result up to rounding order):
+ *
+ *   For every (b, h) and query row i of an [B,H,N,D] row-major tensor set,
+ *     visible(i) = { j : 0 <= j < N }            (non-causal)
+ *                = { j : 0 <= j <= i }           (causal, top-left aligned)
+ *     s_ij   = scale * sum_d q_id * k_jd                  j in visible(i)
+ *     m_i    = max_j s_ij
+ *     p_ij   = exp(s_ij - m_i) / sum_j' exp(s_ij' - m_i)
+ *     o_ic   = sum_j p_ij * v_jc
+ *     lse_i  = m_i + ln sum_j exp(s_ij - m_i)     (natural log, scaled scores)
+ *
+ * Sources:
+ *   - "1 朴素的Attention", §1.1.2 "Attention公式拆解" of the cishoon.github.io
+ *     flashattention page: Attention(Q,K,V) = softmax(QK^T/sqrt(d)) V, the
+ *     safe (max-subtracted) softmax and o_i = sum_j alpha_ij v_j; its §2
+ *     "编写朴素Attention的 cuda 算子" (S, then row softmax, then P V).
+ *   - Causal visibility (key j visible to row i iff j <= i): §1.4 and §3.4 of
+ *     the dandandamowang.xyz "Flash Attention (二) v2" page.
+ *   - Online-softmax recurrence used by attn_oracle_online_fwd: §2 "在线
+ *     Softmax 的数值稳定性" of the chang-wenbin.github.io FA2 report; the
+ *     Br/Bc tiling with causal block skip and diagonal element mask: §3.4 of
+ *     the dandandamowang.xyz page.
+ *
+ * Every function returns 0 on success and a negative value on a bad argument.
+ * All arrays are caller-owned host memory; nothing is retained after return.
+ * nthreads <= 0 means "one thread per CPU in this process's affinity mask".
+ */
+#ifndef ATTN_ORACLE_H
+#define ATTN_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Full forward.  q,k,v: [B,H,N,D] fp64.  o: [B,H,N,D].  lse: [B,H,N] or NULL. */
+int attn_oracle_fwd(const double* q, const double* k, const double* v,
+                    double* o, double* lse,
+                    int64_t B, int64_t H, int64_t N, int64_t D,
+                    double scale, int causal, int nthreads);
+
+/* Selected rows only.  Row r of the request is (bh_idx[r], row_idx[r]) with
+ * bh_idx = b*H + h.  o_rows: [nrows, D].  lse_rows: [nrows] or NULL. */
+int attn_oracle_rows(const double* q, const double* k, const double* v,
+                     int64_t B, int64_t H, int64_t N, int64_t D,
+                     double scale, int causal,
+                     const int64_t* bh_idx, const int64_t* row_idx, int64_t nrows,
+                     double* o_rows, double* lse_rows, int nthreads);
+
+/* Attention probabilities of one head (b*H+h = bh): p: [N, N], row i holds
+ * p_ij for every key j (0 where j is not visible to i). */
+int attn_oracle_probs(const double* q, const double* k,
+                      int64_t B, int64_t H, int64_t N, int64_t D, int64_t bh,
+                      double scale, int causal, double* p);
+
+/* The tiled method itself, restated on the CPU in fp64 in the pages' order:
+ * Q tiles of Br rows outer, K/V tiles of Bc keys inner, running row max m and
+ * sum l, unnormalised accumulator O~ rescaled by exp(m_old - m_new), one
+ * division by l at the end, KV loop cut at min(q_start + Br, N) under causal
+ * masking and the element mask applied on tiles that cross the diagonal.
+ * It exists to pin the tiling algebra (masks, skip bounds, tails) against the
+ * definition above, independently of any GPU code. */
+int attn_oracle_online_fwd(const double* q, const double* k, const double* v,
+                           double* o, double* lse,
+                           int64_t B, int64_t H, int64_t N, int64_t D,
+                           double scale, int causal, int64_t Br, int64_t Bc,
+                           int nthreads);
+
+/* Number of threads nthreads<=0 resolves to (CPUs in the affinity mask). */
+int attn_oracle_default_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,90 @@
+"""Seeded synthetic inputs and the named workloads.
+
+This module holds no attention arithmetic: it only draws Q, K, V from seeded
+generators and names the shapes.  Both the CUDA path and the CPU oracle are fed
+from here, so that the two always see bit-identical inputs.
+
+Recipe: each of Q, K, V is drawn by its own ``torch.Generator('cpu')`` seeded
+with ``seed + 0``, ``seed + 1``, ``seed + 2``, as iid standard normals in fp32,
+multiplied by a per-tensor standard deviation (an exact power-of-two scale
+for the stress workload's Q), then cast to the working dtype with
+round-to-nearest-even (``Tensor.to``).
+"""
+from dataclasses import dataclass, field
+import math
+
+import torch
+
+DTYPES = {"fp32": torch.float32, "fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    D: int
+    dtype: str           # "fp32" | "fp16" | "bf16"
+    causal: bool
+    seed: int
+    q_std: float = 1.0
+    k_std: float = 1.0
+    v_std: float = 1.0
+    note: str = field(default="", compare=False)
+
+    @property
+    def scale(self) -> float:
+        # scale = 1/sqrt(D), rounded once to fp32 and handed unchanged to both
+        # the kernel and the oracle.
+        return float(torch.tensor(1.0 / math.sqrt(self.D), dtype=torch.float32).item())
+
+    @property
+    def torch_dtype(self):
+        return DTYPES[self.dtype]
+
+    def flops(self) -> float:
+        """4*B*H*N^2*D, halved under causal masking (the pages' convention)."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.D
+        return f / 2.0 if self.causal else f
+
+
+# The five workloads of the method's headline study, in order.  The seed of
+# workload i is 1000 + i.
+WORKLOADS = [
+    Workload("fp32_B1_H1_N256_D64", 1, 1, 256, 64, "fp32", False, 1000,
+             note="small fp32 case, non-causal"),
+    Workload("fp32_B4_H8_N8192_D64_causal", 4, 8, 8192, 64, "fp32", True, 1001,
+             note="CUDA-core FFMA path, one row per thread, Br=128, Bc=32"),
+    Workload("bf16_B4_H16_N4096_D128", 4, 16, 4096, 128, "bf16", False, 1002,
+             note="tensor-core path, non-causal (headline)"),
+    Workload("bf16_B2_H32_N8192_D128_causal_qstd4", 2, 32, 8192, 128, "bf16", True, 1003,
+             q_std=4.0, note="causal; Q ~ N(0,16) stresses online-softmax rescaling"),
+    Workload("fp16_B1_H16_N16000_D64_causal", 1, 16, 16000, 64, "fp16", True, 1004,
+             note="causal fp16, long sequence"),
+]
+BY_NAME = {w.name: w for w in WORKLOADS}
+HEADLINE = WORKLOADS[2]
+
+
+def _draw(shape, seed, std, dtype):
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    x = torch.randn(*shape, generator=g, dtype=torch.float32)
+    if std != 1.0:
+        x = x * float(std)
+    return x.to(dtype)
+
+
+def make_qkv(B, H, N, D, dtype="bf16", seed=0, q_std=1.0, k_std=1.0, v_std=1.0):
+    """Host (CPU) tensors q, k, v of shape [B,H,N,D] in the given dtype."""
+    td = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    shape = (B, H, N, D)
+    q = _draw(shape, seed + 0, q_std, td)
+    k = _draw(shape, seed + 1, k_std, td)
+    v = _draw(shape, seed + 2, v_std, td)
+    return q, k, v
+
+
+def workload_inputs(w: Workload):
+    return make_qkv(w.B, w.H, w.N, w.D, w.dtype, w.seed, w.q_std, w.k_std, w.v_std)
