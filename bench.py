@@ -1,0 +1,350 @@
+"""Benchmark of the attention forward on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one attention forward (the whole hot path: one kernel launch) over
+the named workload's synthetic seeded inputs, already resident in HBM.
+Defaults: the headline workload bf16 B=4 H=16 N=4096 D=128 non-causal.
+
+Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
+events on the stream the kernel is launched on; L2 is flushed (a 512 MB
+buffer is rewritten) before every timed step, outside the events.  The whole
+timed loop is bracketed by a barrier and a device synchronise; the reported
+time is the max over ranks.  Under torchrun (N > 1) every rank runs the same
+workload on its own GPU (independent replicas: the method has no exchange
+step), so `value` is the total FLOP of all ranks over that max time.
+
+`e2e` is the same metric measured through the library's host-buffer entry
+point (fattn_fwd_host): per step, the host->device copies of Q, K, V from
+pinned memory, the kernel and the device->host copy of O and LSE.
+
+`cpu_baseline` is the fp64 CPU oracle as it stands, timed on this host's cores
+on a bounded sample of the same workload (a set of random query rows).
+`--impl reference` times that oracle alone (the reference arm of this method).
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from tiled_attention_forward_gb300.inputs import BY_NAME, HEADLINE, workload_inputs  # noqa: E402
+
+METRIC = "attn fwd TFLOP/s (B=4,H=16,N=4096,D=128 bf16) and % of GB300 BF16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+DTYPE_NAMES = {"bf16": "bf16", "fp16": "f16", "fp32": "f32"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def config_of(w, n_gpus):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "dtype": w.dtype,
+            "causal": w.causal, "q_std": w.q_std, "scale": w.scale, "seed": w.seed,
+            "l2": "flushed before every timed step (512 MB rewrite outside the events)",
+            "parallelism": "replicas x%d (no exchange step)" % n_gpus}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [s for (t, s) in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if not inside:  # region shorter than the sampling period: nearest samples
+            near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))[:3]
+            inside = [s for (_, s) in near]
+            window = "nearest samples to a timed region shorter than the 100 ms sampling period"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        sm = [float(s[1]) for s in inside if s[1].replace(".", "").isdigit()]
+        smax = [float(s[2]) for s in inside if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4)
+                          if len(s) > 5 + i and s[5 + i].lower() == "active"})
+        power = [float(s[3]) for s in inside if s[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample (the cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_rows_rate(w, q64, k64, v64, target_s, seed):
+    """Times the oracle on random query rows of the workload; returns
+    (FLOP done in the method's convention, seconds, rows, threads)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    BH = w.B * w.H
+
+    def flops_of(rows):
+        keys = (rows + 1) if w.causal else np.full_like(rows, w.N)
+        return float(np.sum(4.0 * keys * w.D))  # 2 FLOP for q.k and 2 for p.v per key and dim
+
+    def run(nrows):
+        bh = rng.integers(0, BH, nrows)
+        rows = rng.integers(0, w.N, nrows)
+        t = time.perf_counter()
+        oracle.attention_rows(q64, k64, v64, w.scale, w.causal, bh, rows)
+        return time.perf_counter() - t, flops_of(rows)
+
+    nrows = 256
+    dt, fl = run(nrows)
+    while dt < 0.5 and nrows < (1 << 22):
+        nrows *= 4
+        dt, fl = run(nrows)
+    nrows = max(1, int(nrows * target_s / max(dt, 1e-9)))
+    dt, fl = run(nrows)
+    return fl, dt, nrows, oracle.default_threads()
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, w, ws, rank, local):
+    import tiled_attention_forward_gb300 as fattn
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    q, k, v = workload_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fattn.fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream)
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fattn.get_device_status(stream) != 0:
+        raise RuntimeError("device status after warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t1 = time.time()
+    time.sleep(0.15)
+    sampler.stop()
+    status = fattn.get_device_status(stream)
+    if status != 0:
+        raise RuntimeError("device status %s during the timed region" % fattn.status_string(status))
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
+    ms_total = float(sum(per))
+    launches = args.steps  # fattn_fwd launches exactly one kernel per call
+
+    # end to end through the host-buffer entry point
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty_like(q).pin_memory()
+    lh = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        fattn.fwd_host(qh, kh, vh, qd, kd, vd, o, oh, lse, lh, causal=w.causal, scale=w.scale,
+                       stream=stream)
+    torch.cuda.synchronize(dev)
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    es.record(stream)
+    for _ in range(e2e_steps):
+        fattn.fwd_host(qh, kh, vh, qd, kd, vd, o, oh, lse, lh, causal=w.causal, scale=w.scale,
+                       stream=stream)
+    ee.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = es.elapsed_time(ee) / e2e_steps
+    elem = q.element_size()
+    h2d = 3 * q.numel() * elem
+    d2h = o.numel() * elem + lse.numel() * 4
+
+    times = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms_total, e2e_ms = times.tolist()
+    clocks = sampler.summary(t0, t1)
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return None
+
+    flops = w.flops()
+    ms_per_step = ms_total / args.steps
+    value = flops * ws * args.steps / (ms_total * 1e-3) / 1e12
+    achieved = flops / (ms_per_step * 1e-3) / 1e12  # one launch = one step on this GPU
+    peaks, peak_src = load_peaks()
+    peak_key = "bf16_tflops"
+    if w.dtype == "fp32":
+        sm_mhz = peaks.get("sm_max_mhz", 2070.0)
+        peak = torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT,
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": "FP32 FFMA: SMs x 128 lanes x 2 FLOP x max SM clock (%s clock)" % peak_src}
+    else:
+        peak = float(peaks[peak_key])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": "%s dense bf16 (cuBLAS burst) of %s; fp16 taken at the same rate"
+                               % (peak_key, peak_src),
+                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak))}
+    roof["traffic_note"] = "DRAM bytes per launch from ncu: see profiles/"
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_median": statistics.median(per),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": DTYPE_NAMES[w.dtype], "data": "synthetic (seeded iid normal Q, K, V)",
+        "config": config_of(w, ws), "pct_of_peak": 100.0 * roof["frac"], "roofline": roof,
+        "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms, "api": "fattn_fwd_host (pinned host buffers)"},
+        "gpu_launches": launches, "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        q64, k64, v64 = (t.to(torch.float64).numpy() for t in (q, k, v))
+        fl, secs, nrows, threads = oracle_rows_rate(w, q64, k64, v64, args.cpu_seconds, 1)
+        line["cpu_baseline"] = {"value": fl / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": "%d random query rows of the workload (%.1f s, fp64 C "
+                                          "oracle, one thread per CPU)" % (nrows, secs)}
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return line
+
+
+def run_reference(args, w, ws, rank):
+    if rank != 0:
+        return None
+    q, k, v = workload_inputs(w)
+    q64, k64, v64 = (t.to(torch.float64).numpy() for t in (q, k, v))
+    per_step_s = max(0.5, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        oracle_rows_rate(w, q64, k64, v64, min(per_step_s, 1.0), 100 + i)
+    flops_tot, rows_tot, secs_tot, threads = 0.0, 0, 0.0, 1
+    for i in range(args.steps):
+        fl, s, n, threads = oracle_rows_rate(w, q64, k64, v64, per_step_s, 1000 + i)
+        flops_tot += fl
+        rows_tot += n
+        secs_tot += s
+    value = flops_tot / secs_tot / 1e12 if secs_tot > 0 else 0.0
+    sample = "%d random query rows over %d steps (%.1f s), fp64 C oracle" % (rows_tot, args.steps, secs_tot)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs_tot / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded iid normal Q, K, V)",
+        "config": config_of(w, 1),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="wall time of the CPU oracle sample (cpu_baseline)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_env()
+    w = BY_NAME[args.workload]
+    if args.impl == "reference":
+        line = run_reference(args, w, ws, rank)
+    else:
+        line = run_ours(args, w, ws, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

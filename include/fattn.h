@@ -1,0 +1,158 @@
+/*
+ * fattn.h -- C ABI of libfattn: exact scaled-dot-product attention forward on
+ * one NVIDIA GB300 (sm_103a), computed FlashAttention-2 style.
+ *
+ * Operation (the plain definition; cishoon.github.io "flashattention" page,
+ * §1.1.2 "Attention公式拆解"):
+ *
+ *     O = softmax(scale * Q K^T  [+ causal mask]) V
+ *     LSE[i] = ln sum_{j visible to i} exp(scale * q_i . k_j)
+ *
+ * computed without materialising S or P: Q tiles in the outer loop, K/V tiles
+ * streamed in the inner loop, running row max m and row sum l (online
+ * softmax), one 1/l normalisation at the end, and, under causal masking,
+ * K/V tiles wholly above the diagonal skipped and the element mask applied
+ * only on tiles that cross it (dandandamowang.xyz "Flash Attention (二) v2"
+ * page, §1.1-§1.4 and §3.4; online-softmax recurrence: chang-wenbin.github.io
+ * FA2 report, §2).  Causal masking is top-left aligned: key j is visible to
+ * query row i iff j <= i.
+ *
+ * Data layout: every tensor is dense row-major [B, H, N, D] with no padding;
+ * element (b,h,i,d) sits at ((b*H + h)*N + i)*D + d.  LSE is fp32 [B, H, N].
+ * Q, K, V and O share one dtype; the output O has the input dtype.
+ *
+ * Paths: FATTN_BF16 / FATTN_F16 run the tensor-core kernel (TMA, tcgen05 MMA
+ * with TMEM accumulators, fp32 accumulation and softmax, P rounded to the
+ * input dtype for the P.V product).  FATTN_F32 runs a CUDA-core FFMA kernel
+ * (one query row per thread, fp32 throughout).  Supported head dims: 64, 128.
+ *
+ * Ownership: the caller owns every buffer.  No entry point allocates device
+ * or pinned host memory, and nothing is retained after a call returns except
+ * a per-device error word (see fattn_get_device_status).
+ *
+ * Streams: compute entry points are asynchronous on `stream` (a cudaStream_t;
+ * NULL is the legacy default stream).  Argument errors are reported before
+ * anything is enqueued.  An error detected inside a kernel (a bounded wait
+ * that gave up) is recorded in the device error word and surfaces through
+ * fattn_get_device_status.
+ */
+#ifndef FATTN_H
+#define FATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of the shared library are exported explicitly (it is built with
+ * hidden default visibility). */
+#if defined(__GNUC__)
+#define FATTN_API __attribute__((visibility("default")))
+#else
+#define FATTN_API
+#endif
+
+/* A cudaStream_t (the same opaque handle type), without requiring CUDA headers. */
+typedef struct CUstream_st* fattn_stream_t;
+
+typedef enum {
+    FATTN_F32 = 0,
+    FATTN_F16 = 1,
+    FATTN_BF16 = 2
+} fattn_dtype;
+
+typedef enum {
+    FATTN_OK = 0,
+    FATTN_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad dtype, non-finite or negative scale, overlapping O */
+    FATTN_ERR_UNSUPPORTED = 2,   /* D not in {64, 128}; N*D, B*H or N beyond the kernels' index range */
+    FATTN_ERR_MISALIGNED = 3,    /* a tensor pointer not 16-byte aligned (TMA / vector access requirement) */
+    FATTN_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (launch, copy, tensor-map encode) */
+    FATTN_ERR_TIMEOUT = 5,       /* a kernel's bounded wait expired (reported by fattn_get_device_status) */
+    FATTN_ERR_NO_DEVICE = 6      /* no usable sm_103 device is current */
+} fattn_status;
+
+/*
+ * fattn_fwd -- attention forward on device buffers.
+ *
+ *   q, k, v : device pointers, [B,H,N,D] of `dtype`, read only, 16-byte aligned.
+ *   o       : device pointer, [B,H,N,D] of `dtype`, written; must not overlap q/k/v.
+ *   lse     : device pointer to fp32 [B,H,N], written; may be NULL (not written).
+ *   B,H,N,D : sizes; B,H,N >= 0 and D in {64, 128}.  B*H*N == 0 returns FATTN_OK
+ *             with nothing enqueued.
+ *   scale   : multiplier of q.k (typically 1/sqrt(D)); finite and >= 0.
+ *   causal  : 0 = every key visible; nonzero = key j visible to row i iff j <= i.
+ *   dtype   : a fattn_dtype.
+ *   stream  : CUDA stream the single kernel launch is enqueued on.
+ *
+ * Returns FATTN_OK once the kernel is enqueued, or an error code (nothing
+ * enqueued on argument errors).  Exactly one kernel is launched per call.
+ */
+FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+              int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal,
+              int dtype, fattn_stream_t stream);
+
+/*
+ * fattn_fwd_host -- the same forward for callers holding the tensors in host
+ * memory: enqueues on `stream` the host->device copies of q, k, v into the
+ * caller's device buffers q_dev, k_dev, v_dev, the forward kernel writing
+ * o_dev / lse_dev, and the device->host copies of O (and LSE when both
+ * lse_host and lse_dev are non-NULL) into o_host / lse_host.  One
+ * cudaMemcpyAsync per tensor.  Host buffers should be page-locked for the
+ * copies to be asynchronous; the call returns once everything is enqueued, so
+ * the caller synchronises `stream` before reading o_host.  Argument rules are
+ * those of fattn_fwd, applied to the device buffers; host pointers must be
+ * non-NULL.
+ */
+FATTN_API int fattn_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                   void* o_host, float* lse_host,
+                   void* q_dev, void* k_dev, void* v_dev, void* o_dev, float* lse_dev,
+                   int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal,
+                   int dtype, fattn_stream_t stream);
+
+/*
+ * fattn_plan -- host-only description of the launch fattn_fwd would make for
+ * these arguments (no CUDA call when num_sms > 0).  Fills `out` with:
+ *   out[0] path       : 0 = none (empty problem), 1 = FFMA fp32, 2 = tcgen05 bf16/fp16
+ *   out[1] grid_x     : CTAs launched (x)
+ *   out[2] grid_y     : CTAs launched (y)
+ *   out[3] threads    : threads per CTA
+ *   out[4] smem_bytes : dynamic shared memory per CTA
+ *   out[5] tasks      : work units (one Q tile of one head; BM = 256 rows on
+ *                       the tcgen05 path, Br = 128 rows on the FFMA path)
+ *   out[6] kv_tiles   : K/V tiles visited over all tasks (causal skip applied)
+ *   out[7] rows_per_task, out[8] keys_per_kv_tile
+ * num_sms <= 0 queries the current device.  Returns a fattn_status.
+ */
+FATTN_API int fattn_plan(int64_t B, int64_t H, int64_t N, int64_t D, int causal, int dtype,
+               int num_sms, int64_t out[9]);
+
+/*
+ * fattn_get_device_status -- synchronises `stream`, then reads and clears the
+ * current device's error word.  Returns FATTN_OK, FATTN_ERR_TIMEOUT if a
+ * kernel gave up a bounded wait since the last call, or FATTN_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+FATTN_API int fattn_get_device_status(fattn_stream_t stream);
+
+/*
+ * fattn_selftest_wait_timeout -- launches one tiny kernel whose single thread
+ * waits, with the same bounded wait the forward kernels use, on a shared
+ * memory barrier that nothing ever completes; after `timeout_ns` it records
+ * FATTN_ERR_TIMEOUT in the device error word and returns.  Exists so the
+ * timeout path can be exercised without hanging or faulting a GPU.
+ * timeout_ns must be in (0, 10^9].  Asynchronous on `stream`.
+ */
+FATTN_API int fattn_selftest_wait_timeout(uint64_t timeout_ns, fattn_stream_t stream);
+
+/* Human-readable name of a fattn_status (static string, never NULL). */
+FATTN_API const char* fattn_status_string(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+FATTN_API int fattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FATTN_H */

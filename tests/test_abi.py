@@ -1,0 +1,182 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol
+include/fattn.h declares, rejects bad arguments before touching CUDA, and
+plans launches with the tile arithmetic the pages print."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+import torch
+
+import tiled_attention_forward_gb300 as fattn
+from tiled_attention_forward_gb300 import build as fbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fattn.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA_ERR, TIMEOUT, NO_DEVICE = range(7)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(fbuild.LIB):
+        fbuild.build()
+    return fattn.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"FATTN_API\s+[\w\s\*]*?\b(fattn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("fattn_fwd", "fattn_fwd_host", "fattn_plan", "fattn_get_device_status",
+                 "fattn_selftest_wait_timeout", "fattn_status_string", "fattn_version"):
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings(lib):
+    for code, name in fattn.STATUS.items():
+        assert fattn.status_string(code) == name
+    assert fattn.status_string(99) == "FATTN_ERR_UNKNOWN"
+    assert lib.fattn_version() == 10000
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address that is never dereferenced
+
+
+def call_fwd(lib, q=FAKE, k=FAKE + (1 << 16), v=FAKE + (2 << 16), o=FAKE + (3 << 16), lse=None,
+             B=1, H=1, N=16, D=64, scale=0.125, causal=0, dtype=2):
+    return lib.fattn_fwd(q, k, v, o, lse, B, H, N, D, scale, causal, dtype, None)
+
+
+def test_argument_errors_before_any_cuda_call(lib):
+    assert call_fwd(lib, q=None) == INVALID
+    assert call_fwd(lib, o=None) == INVALID
+    assert call_fwd(lib, B=-1) == INVALID
+    assert call_fwd(lib, N=-5) == INVALID
+    assert call_fwd(lib, dtype=7) == INVALID
+    assert call_fwd(lib, scale=float("nan")) == INVALID
+    assert call_fwd(lib, scale=float("inf")) == INVALID
+    assert call_fwd(lib, scale=-1.0) == INVALID
+    assert call_fwd(lib, D=96) == UNSUPPORTED
+    assert call_fwd(lib, D=256) == UNSUPPORTED
+    assert call_fwd(lib, q=FAKE + 8) == MISALIGNED
+    assert call_fwd(lib, o=FAKE + (3 << 16) + 2) == MISALIGNED
+    assert call_fwd(lib, lse=FAKE + (4 << 16) + 1) == MISALIGNED
+    # O overlapping an input, LSE overlapping O
+    assert call_fwd(lib, o=FAKE + 16) == INVALID
+    assert call_fwd(lib, lse=FAKE + (3 << 16) + 64) == INVALID
+    # index range limits
+    assert call_fwd(lib, N=(1 << 30) + 1) == UNSUPPORTED
+    assert call_fwd(lib, B=1 << 16, H=1 << 16) == UNSUPPORTED
+    assert call_fwd(lib, B=70000, H=1, dtype=0) == UNSUPPORTED
+
+
+def test_empty_problem_is_ok_and_enqueues_nothing(lib):
+    for (B, H, N) in ((0, 4, 16), (2, 0, 16), (2, 4, 0)):
+        assert call_fwd(lib, q=None, k=None, v=None, o=None, B=B, H=H, N=N) == OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_call_without_a_device_reports_no_device(lib):
+    assert call_fwd(lib) == NO_DEVICE
+    assert call_fwd(lib, dtype=0) == NO_DEVICE
+    assert lib.fattn_selftest_wait_timeout(1000, None) == NO_DEVICE
+    assert lib.fattn_selftest_wait_timeout(0, None) == INVALID
+
+
+def test_host_entry_point_argument_errors(lib):
+    args = [FAKE, FAKE, FAKE, FAKE + (5 << 16), None,
+            FAKE, FAKE + (1 << 16), FAKE + (2 << 16), FAKE + (3 << 16), None,
+            1, 1, 16, 64, 0.125, 0, 2, None]
+    bad = list(args)
+    bad[0] = None
+    assert lib.fattn_fwd_host(*bad) == INVALID
+    bad = list(args)
+    bad[8] = None
+    assert lib.fattn_fwd_host(*bad) == INVALID
+    bad = list(args)
+    bad[13] = 80
+    assert lib.fattn_fwd_host(*bad) == UNSUPPORTED
+
+
+def test_plan_ffma_matches_page_tile_arithmetic(lib, golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "tile_arithmetic.json")))
+    grid = g["cases"][0]
+    # fp32 path: grid = (ceil(N/Br), B*H) with Br = 128
+    p = fattn.plan(4, 8, grid["N"], 64, causal=False, dtype=torch.float32, num_sms=152)
+    assert p["path"] == 1
+    assert (p["grid_x"], p["grid_y"]) == (grid["grid_x"], grid["grid_y"])
+    assert p["grid_x"] * p["grid_y"] == grid["blocks"]
+    assert p["rows_per_task"] == grid["Br"] and p["threads"] == grid["Br"]
+    nvec = g["cases"][1]
+    assert p["keys_per_kv_tile"] == nvec["Bc"]
+    assert nvec["Bc"] * nvec["D"] * nvec["elem_bytes"] // 16 == nvec["nvec"]
+    # non-causal: every Q block visits every K/V tile
+    assert p["kv_tiles"] == 64 * 32 * (8192 // 32)
+
+
+def test_plan_causal_skip_counts(lib, golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "tile_arithmetic.json")))["cases"][2]
+    N, Br, Bc = g["N"], g["Br"], g["Bc"]
+    p = fattn.plan(1, 1, N, 64, causal=True, dtype=torch.float32, num_sms=152)
+    nq = N // Br
+    # Q block qb visits ceil(min((qb+1)*Br, N)/Bc) tiles; block 5 visits 24 and skips 40
+    per_block = [min((qb + 1) * Br, N) // Bc for qb in range(nq)]
+    assert per_block[g["q_block"]] == g["tiles_visited"]
+    assert N // Bc - per_block[g["q_block"]] == g["tiles_skipped"]
+    assert p["kv_tiles"] == sum(per_block)
+
+
+def test_plan_tensor_core_path(lib):
+    p = fattn.plan(4, 16, 4096, 128, causal=False, dtype=torch.bfloat16, num_sms=152)
+    assert p["path"] == 2
+    assert p["tasks"] == 4 * 16 * (4096 // 256)
+    assert p["grid_x"] == 152 and p["grid_y"] == 1
+    assert p["rows_per_task"] == 256 and p["keys_per_kv_tile"] == 128
+    assert p["kv_tiles"] == p["tasks"] * (4096 // 128)
+    assert p["smem_bytes"] <= 227 * 1024
+    # causal N=16000: the last task's second Q tile starts at row 16000 (empty)
+    p = fattn.plan(1, 16, 16000, 64, causal=True, dtype=torch.float16, num_sms=152)
+    nq = -(-16000 // 256)
+    assert p["tasks"] == 16 * nq
+    tiles = sum(max(min(qb * 256 + 128, 16000) // 128 if qb * 256 < 16000 else 0,
+                    (-(-min(qb * 256 + 256, 16000) // 128)) if qb * 256 + 128 < 16000 else 0)
+                for qb in range(nq))
+    assert p["kv_tiles"] == 16 * tiles
+    # few tasks: one CTA per task
+    p = fattn.plan(1, 1, 256, 64, causal=False, dtype=torch.bfloat16, num_sms=152)
+    assert p["tasks"] == 1 and p["grid_x"] == 1
+
+
+def test_plan_errors(lib):
+    with pytest.raises(fattn.FattnError):
+        fattn.plan(1, 1, 16, 80)
+    assert fattn.plan(0, 1, 16, 64, num_sms=152)["path"] == 0
+
+
+def test_product_path_does_not_touch_the_oracle():
+    """The binding and the library never import or link the CPU oracle."""
+    pkg = os.path.dirname(fattn.__file__)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "attn_oracle" not in text, f
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(fattn, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(fattn, "_lib", None)
+    with pytest.raises(fattn.FattnLibraryMissing):
+        fattn.load()

@@ -1,0 +1,182 @@
+"""tiled_attention_forward_gb300 -- Python binding of libfattn.
+
+Exact scaled-dot-product attention forward on one GB300 (sm_103a), computed
+FlashAttention-2 style by hand-written CUDA kernels behind a C ABI
+(``include/fattn.h``).  This module only marshals arguments: it turns torch
+tensors into device pointers and the current CUDA stream into a
+``cudaStream_t`` and calls the library.  Every step of the computation runs in
+the library's kernels; there is no fallback of any kind.  If ``libfattn.so``
+has not been built (``python -m tiled_attention_forward_gb300.build``), every
+call raises ``FattnLibraryMissing``.
+
+    import torch, tiled_attention_forward_gb300 as fattn
+    o, lse = fattn.fwd(q, k, v, causal=True)     # q,k,v: [B,H,N,D] cuda tensors
+"""
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = ["fwd", "fwd_host", "plan", "get_device_status", "selftest_wait_timeout",
+           "status_string", "library_path", "load", "FattnError", "FattnLibraryMissing",
+           "DTYPE_CODES", "STATUS"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libfattn.so")
+
+DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+STATUS = {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPORTED",
+          3: "FATTN_ERR_MISALIGNED", 4: "FATTN_ERR_CUDA", 5: "FATTN_ERR_TIMEOUT",
+          6: "FATTN_ERR_NO_DEVICE"}
+PLAN_FIELDS = ("path", "grid_x", "grid_y", "threads", "smem_bytes", "tasks", "kv_tiles",
+               "rows_per_task", "keys_per_kv_tile")
+
+
+class FattnError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__("%s returned %s (%d)" % (where, STATUS.get(code, "?"), code))
+
+
+class FattnLibraryMissing(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def load():
+    """Load libfattn.so (once).  Raises FattnLibraryMissing if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise FattnLibraryMissing(
+            "libfattn.so is not built at %s; run `python -m tiled_attention_forward_gb300.build`"
+            % _LIB_PATH)
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i64, f32, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+    lib.fattn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, ci, ci, vp]
+    lib.fattn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                   i64, i64, i64, i64, f32, ci, ci, vp]
+    lib.fattn_plan.argtypes = [i64, i64, i64, i64, ci, ci, ci, ctypes.POINTER(i64)]
+    lib.fattn_get_device_status.argtypes = [vp]
+    lib.fattn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    lib.fattn_status_string.argtypes = [ci]
+    lib.fattn_status_string.restype = ctypes.c_char_p
+    lib.fattn_version.argtypes = []
+    for f in ("fattn_fwd", "fattn_fwd_host", "fattn_plan", "fattn_get_device_status",
+              "fattn_selftest_wait_timeout", "fattn_version"):
+        getattr(lib, f).restype = ci
+    _lib = lib
+    return lib
+
+
+def status_string(code):
+    return load().fattn_status_string(int(code)).decode()
+
+
+def _check(code, where):
+    if code != 0:
+        raise FattnError(code, where)
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _default_scale(D):
+    # 1/sqrt(D) rounded once to fp32, the value the library multiplies by.
+    return float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32).item())
+
+
+def _check_qkv(q, k, v):
+    if q.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, D]")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must have the same dtype")
+    if q.dtype not in DTYPE_CODES:
+        raise ValueError("dtype must be float32, float16 or bfloat16")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous row-major [B, H, N, D]")
+
+
+def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, return_lse=True, stream=None):
+    """Attention forward on CUDA tensors.
+
+    q, k, v: [B, H, N, D] contiguous CUDA tensors of one dtype (float32,
+    float16 or bfloat16), D in {64, 128}.  Returns (o, lse): o has q's dtype
+    and shape; lse is float32 [B, H, N] (natural-log log-sum-exp of the
+    scaled scores), or None when return_lse is False.  ``out`` / ``lse`` may
+    be given to write into existing tensors.  Enqueued on ``stream`` (default:
+    torch's current stream); no synchronisation.
+    """
+    _check_qkv(q, k, v)
+    if not q.is_cuda:
+        raise ValueError("fwd needs CUDA tensors; see fwd_host for host buffers")
+    B, H, N, D = q.shape
+    if scale is None:
+        scale = _default_scale(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    lse_ptr = lse.data_ptr() if (return_lse and lse is not None) else None
+    lib = load()
+    with torch.cuda.device(q.device):
+        rc = lib.fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
+                           B, H, N, D, float(scale), int(bool(causal)), DTYPE_CODES[q.dtype],
+                           _stream_handle(stream))
+    _check(rc, "fattn_fwd")
+    return out, (lse if return_lse else None)
+
+
+def fwd_host(q_host, k_host, v_host, q_dev, k_dev, v_dev, o_dev, o_host, lse_dev=None,
+             lse_host=None, causal=False, scale=None, stream=None):
+    """End-to-end forward from host tensors: host->device copies, the kernel and
+    the device->host copy of O (and LSE) are all enqueued by the library on
+    ``stream``.  Host tensors should be pinned; the caller synchronises."""
+    _check_qkv(q_host, k_host, v_host)
+    B, H, N, D = q_host.shape
+    if scale is None:
+        scale = _default_scale(D)
+    lib = load()
+    with torch.cuda.device(q_dev.device):
+        rc = lib.fattn_fwd_host(q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(),
+                                o_host.data_ptr(),
+                                lse_host.data_ptr() if lse_host is not None else None,
+                                q_dev.data_ptr(), k_dev.data_ptr(), v_dev.data_ptr(),
+                                o_dev.data_ptr(),
+                                lse_dev.data_ptr() if lse_dev is not None else None,
+                                B, H, N, D, float(scale), int(bool(causal)),
+                                DTYPE_CODES[q_host.dtype], _stream_handle(stream))
+    _check(rc, "fattn_fwd_host")
+
+
+def plan(B, H, N, D, causal=False, dtype=torch.bfloat16, num_sms=0):
+    """Launch plan (host only when num_sms > 0) as a dict; see fattn_plan."""
+    out = (ctypes.c_int64 * 9)()
+    code = DTYPE_CODES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    rc = load().fattn_plan(B, H, N, D, int(bool(causal)), code, int(num_sms), out)
+    _check(rc, "fattn_plan")
+    return dict(zip(PLAN_FIELDS, list(out)))
+
+
+def get_device_status(stream=None):
+    """Synchronise the stream and return (and clear) the device error word."""
+    return load().fattn_get_device_status(_stream_handle(stream))
+
+
+def selftest_wait_timeout(timeout_ns, stream=None):
+    rc = load().fattn_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream))
+    _check(rc, "fattn_selftest_wait_timeout")

@@ -1,0 +1,280 @@
+// fattn_api.cu -- the C ABI of libfattn (declared in include/fattn.h):
+// argument validation, launch planning, TMA tensor-map encoding and dispatch
+// to the tensor-core (bf16/fp16) or CUDA-core (fp32) kernel.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <cudaTypedefs.h>
+
+#include "fattn.h"
+#include "internal.h"
+
+namespace fattn {
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per barrier wait
+constexpr float kLog2e = 1.4426950408889634f;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u; }
+
+size_t elem_bytes(int dtype) { return dtype == FATTN_F32 ? 4u : 2u; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// Validation shared by every compute entry point; returns FATTN_OK when the
+// call may proceed (which includes the empty problem, flagged by *empty).
+int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             int64_t B, int64_t H, int64_t N, int64_t D, float scale, int dtype, bool* empty) {
+    *empty = false;
+    if (dtype != FATTN_F32 && dtype != FATTN_F16 && dtype != FATTN_BF16) return FATTN_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || N < 0 || D < 0) return FATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || scale < 0.f) return FATTN_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FATTN_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || N == 0) {
+        *empty = true;
+        return FATTN_OK;
+    }
+    // Index ranges: N and B*H fit int32 (kernel indices, TMA coordinates,
+    // grid.y <= 65535 on the FFMA path) and B*H*N*D stays well inside int64.
+    if (N > (int64_t(1) << 30) || B > (int64_t(1) << 30) || H > (int64_t(1) << 30))
+        return FATTN_ERR_UNSUPPORTED;
+    const int64_t BH = B * H;
+    if (BH > (int64_t(1) << 30)) return FATTN_ERR_UNSUPPORTED;
+    if (dtype == FATTN_F32 && BH > 65535) return FATTN_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !o) return FATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FATTN_ERR_MISALIGNED;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FATTN_ERR_MISALIGNED;
+    const size_t bytes = static_cast<size_t>(BH * N * D) * elem_bytes(dtype);
+    if (overlaps(o, bytes, q, bytes) || overlaps(o, bytes, k, bytes) || overlaps(o, bytes, v, bytes))
+        return FATTN_ERR_INVALID_ARG;
+    if (lse) {
+        const size_t lb = static_cast<size_t>(BH * N) * sizeof(float);
+        if (overlaps(lse, lb, o, bytes) || overlaps(lse, lb, q, bytes) || overlaps(lse, lb, k, bytes) ||
+            overlaps(lse, lb, v, bytes))
+            return FATTN_ERR_INVALID_ARG;
+    }
+    return FATTN_OK;
+}
+
+int current_sm_count(int* sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FATTN_ERR_NO_DEVICE;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return FATTN_ERR_NO_DEVICE;
+    if (major != 10 || minor != 3) return FATTN_ERR_NO_DEVICE;  // built for sm_103a only
+    return FATTN_OK;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// K/V tiles one task visits: Q rows [r0, r0+rows) against keys, Bc-key tiles.
+int64_t kv_tiles_for(int64_t r0, int64_t rows, int64_t N, int64_t bc, bool causal) {
+    if (r0 >= N) return 0;
+    const int64_t kv_limit = causal ? std::min(r0 + rows, N) : N;
+    return ceil_div(kv_limit, bc);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qres;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &qres) == cudaSuccess &&
+            qres == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+cudaError_t tc_encode_maps(TcArgs& a, const void* q, const void* k, const void* v, int64_t BH,
+                           int64_t N, int64_t D, bool bf16) {
+    auto encode = get_encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    const CUtensorMapDataType dt =
+        bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    // [B*H][N][D] row-major, 16-bit: innermost D, then rows, then heads.
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 2), static_cast<cuuint64_t>(N * D * 2)};
+    const cuuint32_t box[3] = {64, 128, 1};  // one 128-byte swizzle atom wide, 128 rows
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const void* ptrs[3] = {q, k, v};
+    CUtensorMap* maps[3] = {&a.tmap_q, &a.tmap_k, &a.tmap_v};
+    for (int i = 0; i < 3; ++i) {
+        CUresult r = encode(maps[i], dt, 3, const_cast<void*>(ptrs[i]), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace fattn
+
+using namespace fattn;
+
+extern "C" {
+
+int fattn_version(void) { return 10000; }
+
+const char* fattn_status_string(int status) {
+    switch (status) {
+        case FATTN_OK: return "FATTN_OK";
+        case FATTN_ERR_INVALID_ARG: return "FATTN_ERR_INVALID_ARG";
+        case FATTN_ERR_UNSUPPORTED: return "FATTN_ERR_UNSUPPORTED";
+        case FATTN_ERR_MISALIGNED: return "FATTN_ERR_MISALIGNED";
+        case FATTN_ERR_CUDA: return "FATTN_ERR_CUDA";
+        case FATTN_ERR_TIMEOUT: return "FATTN_ERR_TIMEOUT";
+        case FATTN_ERR_NO_DEVICE: return "FATTN_ERR_NO_DEVICE";
+        default: return "FATTN_ERR_UNKNOWN";
+    }
+}
+
+int fattn_plan(int64_t B, int64_t H, int64_t N, int64_t D, int causal, int dtype, int num_sms,
+               int64_t out[9]) {
+    if (!out) return FATTN_ERR_INVALID_ARG;
+    for (int i = 0; i < 9; ++i) out[i] = 0;
+    if (dtype != FATTN_F32 && dtype != FATTN_F16 && dtype != FATTN_BF16) return FATTN_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || N < 0 || D < 0) return FATTN_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FATTN_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || N == 0) return FATTN_OK;
+    if (N > (int64_t(1) << 30) || B > (int64_t(1) << 30) || H > (int64_t(1) << 30) ||
+        B * H > (int64_t(1) << 30))
+        return FATTN_ERR_UNSUPPORTED;
+    const int64_t BH = B * H;
+    const bool c = causal != 0;
+    if (dtype == FATTN_F32) {
+        const int64_t bc = ffma_bc(static_cast<int>(D));
+        const int64_t nq = ceil_div(N, kFfmaBr);
+        int64_t tiles = 0;
+        for (int64_t qb = 0; qb < nq; ++qb) tiles += kv_tiles_for(qb * kFfmaBr, kFfmaBr, N, bc, c);
+        out[0] = 1;
+        out[1] = nq;
+        out[2] = BH;
+        out[3] = kFfmaBr;
+        out[4] = ffma_smem_bytes(static_cast<int>(D));
+        out[5] = nq * BH;
+        out[6] = tiles * BH;
+        out[7] = kFfmaBr;
+        out[8] = bc;
+        return FATTN_OK;
+    }
+    if (num_sms <= 0) {
+        int st = current_sm_count(&num_sms);
+        if (st != FATTN_OK) return st;
+    }
+    const int64_t rows = int64_t(kTcBM) * kTcQTiles;
+    const int64_t nq = ceil_div(N, rows);
+    int64_t tiles = 0;
+    for (int64_t qb = 0; qb < nq; ++qb) {
+        const int64_t t0 = kv_tiles_for(qb * rows, kTcBM, N, kTcBN, c);
+        const int64_t t1 = kv_tiles_for(qb * rows + kTcBM, kTcBM, N, kTcBN, c);
+        tiles += std::max(t0, t1);  // the CTA streams each K/V tile once for both Q tiles
+    }
+    const int64_t tasks = nq * BH;
+    out[0] = 2;
+    out[1] = std::min<int64_t>(tasks, num_sms);
+    out[2] = 1;
+    out[3] = kTcThreads;
+    out[4] = tc_smem_bytes(static_cast<int>(D));
+    out[5] = tasks;
+    out[6] = tiles * BH;
+    out[7] = rows;
+    out[8] = kTcBN;
+    return FATTN_OK;
+}
+
+int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+              int64_t N, int64_t D, float scale, int causal, int dtype, fattn_stream_t stream_h) {
+    bool empty = false;
+    int st = validate(q, k, v, o, lse, B, H, N, D, scale, dtype, &empty);
+    if (st != FATTN_OK || empty) return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
+    const int64_t BH = B * H;
+    const float scale_log2 = scale * kLog2e;
+
+    if (dtype == FATTN_F32) {
+        int sms = 0;
+        st = current_sm_count(&sms);
+        if (st != FATTN_OK) return st;
+        cudaError_t e = ffma_launch(static_cast<const float*>(q), static_cast<const float*>(k),
+                                    static_cast<const float*>(v), static_cast<float*>(o), lse, BH, N,
+                                    D, scale_log2, causal != 0, stream);
+        return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+    }
+
+    int sms = 0;
+    st = current_sm_count(&sms);
+    if (st != FATTN_OK) return st;
+    TcArgs a;
+    std::memset(&a, 0, sizeof(a));
+    const bool bf16 = dtype == FATTN_BF16;
+    if (tc_encode_maps(a, q, k, v, BH, N, D, bf16) != cudaSuccess) return FATTN_ERR_CUDA;
+    a.o = o;
+    a.lse = lse;
+    a.N = static_cast<int>(N);
+    a.BH = static_cast<int>(BH);
+    a.num_qblk = static_cast<int>(ceil_div(N, int64_t(kTcBM) * kTcQTiles));
+    a.num_tasks = a.num_qblk * a.BH;
+    a.scale_log2 = scale_log2;
+    a.timeout_ns = kDefaultTimeoutNs;
+    const int grid = static_cast<int>(std::min<int64_t>(a.num_tasks, sms));
+    cudaError_t e = tc_launch(a, static_cast<int>(D), bf16, causal != 0, grid, stream);
+    return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
+int fattn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                   float* lse_host, void* q_dev, void* k_dev, void* v_dev, void* o_dev, float* lse_dev,
+                   int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal, int dtype,
+                   fattn_stream_t stream_h) {
+    bool empty = false;
+    int st = validate(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, N, D, scale, dtype, &empty);
+    if (st != FATTN_OK || empty) return st;
+    if (!q_host || !k_host || !v_host || !o_host) return FATTN_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
+    const size_t bytes = static_cast<size_t>(B * H * N * D) * elem_bytes(dtype);
+    if (cudaMemcpyAsync(q_dev, q_host, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(k_dev, k_host, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(v_dev, v_host, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return FATTN_ERR_CUDA;
+    st = fattn_fwd(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, N, D, scale, causal, dtype, stream_h);
+    if (st != FATTN_OK) return st;
+    if (cudaMemcpyAsync(o_host, o_dev, bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return FATTN_ERR_CUDA;
+    if (lse_host && lse_dev &&
+        cudaMemcpyAsync(lse_host, lse_dev, static_cast<size_t>(B * H * N) * sizeof(float),
+                        cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return FATTN_ERR_CUDA;
+    return FATTN_OK;
+}
+
+int fattn_get_device_status(fattn_stream_t stream_h) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FATTN_ERR_CUDA;
+    uint32_t word = 0;
+    if (read_and_clear_error_word(&word) != cudaSuccess) return FATTN_ERR_CUDA;
+    if (word & (1u << FATTN_ERR_TIMEOUT)) return FATTN_ERR_TIMEOUT;
+    return FATTN_OK;
+}
+
+int fattn_selftest_wait_timeout(uint64_t timeout_ns, fattn_stream_t stream_h) {
+    if (timeout_ns == 0 || timeout_ns > 1000000000ull) return FATTN_ERR_INVALID_ARG;
+    int sms = 0;
+    int st = current_sm_count(&sms);
+    if (st != FATTN_OK) return st;
+    cudaError_t e = launch_wait_selftest(timeout_ns, reinterpret_cast<cudaStream_t>(stream_h));
+    return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,610 @@
+// fwd_tc.cu -- tensor-core attention forward for bf16 / fp16 on sm_103a.
+//
+// FlashAttention-2 structure (dandandamowang.xyz "Flash Attention (二) v2"
+// page, §1.1-§1.4: Q tile outer, K/V tiles inner, running max/sum on chip,
+// deferred 1/l, causal block skip + diagonal element mask), mapped onto
+// Blackwell's tensor-core machinery in the way the hjcheng0602.cn
+// "flashattn_G7" page describes for SM103 (1-CTA tcgen05, S and O in TMEM,
+// P.V issued in the TS form with P in TMEM, V landed by TMA directly in the
+// MN-major 128-byte-swizzled operand layout, persistent CTAs).
+//
+// One CTA per SM, persistent over tasks.  A task is one (batch*head, 256-row
+// Q block): two 128-row Q tiles that share every K/V tile the CTA streams.
+//
+// Warp roles (384 threads = three warpgroups):
+//   warps 0-3  softmax warpgroup 0: Q tile 0, thread t owns query row t
+//              (TMEM lane t): S row -> mask -> max -> exp2 -> P (16-bit) into
+//              TMEM, conditional O rescale, epilogue (O/l, LSE, store)
+//   warps 4-7  softmax warpgroup 1: same for Q tile 1
+//   warp 8     MMA issue (one thread): S_i = Q_i K_j^T (SS form),
+//              O_i += P_i V_j (TS form), tcgen05.commit -> mbarriers
+//   warp 9     TMA producer (one thread): Q tiles once per task, K/V tiles
+//              through a ring of shared-memory stages
+//   warps 10-11 idle
+// The control warpgroup (warps 8-11) gives up registers (setmaxnreg) so the
+// softmax warpgroups can hold a whole 128-score row per thread: 168 per
+// thread at launch; 2 x 128 x kSoftmaxRegs + 128 x kControlRegs <= 384 x 168.
+//
+// TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
+// O_0 [256,256+D), O_1 [256+D,256+2D).  P_i (two 16-bit values per column)
+// overwrites the first 64 columns of S_i once its scores are in registers.
+//
+// MMA issue order per K/V tile j (tensor-core instructions of one CTA execute
+// in issue order):  PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).  So while softmax
+// warpgroup 0 works on S_0(j+1), the tensor core runs PV_1(j) and S_1(j+1),
+// and vice versa.  A commit after S_i(j+1) fires only once PV_i(j) is done,
+// which is what lets the softmax warpgroup rescale O_i right after it sees
+// S_i(j+1).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fattn {
+
+// Bit k set <=> a kernel on this device hit fattn_status k (only TIMEOUT today).
+__device__ uint32_t g_error_word;
+
+namespace {
+
+constexpr uint32_t kSoftmaxRegs = 208;
+constexpr uint32_t kControlRegs = 80;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kTcThreads * 168,
+              "register split must fit the launch allocation");
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 while the max is stale
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct TcLayout {
+    static constexpr int kAtoms = D / 64;               // 128-byte swizzle atoms along D
+    static constexpr int kAtomRowBytes = 128;           // 64 x 16-bit
+    static constexpr int kQTileBytes = kTcBM * D * 2;
+    static constexpr int kKVTileBytes = kTcBN * D * 2;
+    static constexpr int kStages = (D == 128) ? 5 : 8;  // K/V ring depth
+    static constexpr int kQOff = 0;
+    static constexpr int kKVOff = kTcQTiles * kQTileBytes;
+    static constexpr int kBarOff = kKVOff + kStages * kKVTileBytes;
+    // q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] drain[1]
+    static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kBytes = kMiscOff + 16;
+    static constexpr int kAlloc = kBytes + 1024;        // slack to align the base to 1024 B
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+    static_assert(256 + 2 * D <= 512, "TMEM budget");
+};
+
+struct Task {
+    int bh;
+    int q0;
+    int nb[2];  // K/V tiles visited by Q tile 0 / 1 (0: tile has no valid row)
+    int nbmax;
+};
+
+// Task order: non-causal, head-major (all Q blocks of one head are adjacent so
+// concurrently running CTAs share that head's K/V in L2).  Causal, longest
+// first: Q blocks nearest the end of the sequence (most K/V tiles) are
+// scheduled first, heads inner.
+template <bool CAUSAL>
+__device__ __forceinline__ Task decode_task(int t, const TcArgs& a) {
+    Task k;
+    int qblk;
+    if (CAUSAL) {
+        qblk = a.num_qblk - 1 - t / a.BH;
+        k.bh = t % a.BH;
+    } else {
+        qblk = t % a.num_qblk;
+        k.bh = t / a.num_qblk;
+    }
+    k.q0 = qblk * (kTcBM * kTcQTiles);
+    const int all = (a.N + kTcBN - 1) / kTcBN;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int r0 = k.q0 + i * kTcBM;  // first row of tile i
+        if (r0 >= a.N) {
+            k.nb[i] = 0;
+        } else if (CAUSAL) {
+            const int kv_limit = min(r0 + kTcBM, a.N);  // keys beyond the tile's last row are never visible
+            k.nb[i] = (kv_limit + kTcBN - 1) / kTcBN;
+        } else {
+            k.nb[i] = all;
+        }
+    }
+    k.nbmax = max(k.nb[0], k.nb[1]);
+    return k;
+}
+
+struct Bars {
+    uint64_t* q_full;
+    uint64_t* q_empty;
+    uint64_t* kv_full;
+    uint64_t* kv_empty;
+    uint64_t* s_full;
+    uint64_t* p_full;
+    uint64_t* o_full;
+    uint64_t* drain;
+};
+
+template <int D>
+__device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
+    using L = TcLayout<D>;
+    uint64_t* b = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+    Bars r;
+    r.q_full = b;
+    r.q_empty = b + 2;
+    r.kv_full = b + 4;
+    r.kv_empty = r.kv_full + L::kStages;
+    r.s_full = r.kv_empty + L::kStages;
+    r.p_full = r.s_full + 2;
+    r.o_full = r.p_full + 2;
+    r.drain = r.o_full + 2;
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
+    if (bf16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// TMA producer (one thread)
+// ---------------------------------------------------------------------------
+template <int D, bool CAUSAL>
+__device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
+                              volatile uint32_t* abort_flag) {
+    using L = TcLayout<D>;
+    uint32_t kv_it = 0;
+    uint32_t qcnt[2] = {0u, 0u};
+    bool ok = true;
+    const uint64_t keep = l2_policy_evict_last();   // K/V: re-read by the other Q blocks of the head
+    const uint64_t once = l2_policy_evict_first();  // Q: read once
+
+    auto load_q = [&](int i, const Task& tk) {
+        ok = mbar_wait_bounded(&bars.q_empty[i], (qcnt[i] & 1u) ^ 1u, abort_flag, &g_error_word,
+                               a.timeout_ns);
+        if (!ok) return;
+        mbar_arrive_expect_tx(&bars.q_full[i], L::kQTileBytes);
+        uint8_t* dst = smem + L::kQOff + i * L::kQTileBytes;
+#pragma unroll
+        for (int at = 0; at < L::kAtoms; ++at)
+            tma_load_3d_hint(dst + at * kTcBM * L::kAtomRowBytes, &a.tmap_q, &bars.q_full[i],
+                             at * 64, tk.q0 + i * kTcBM, tk.bh, once);
+        ++qcnt[i];
+    };
+    auto load_kv = [&](const CUtensorMap* map, int j, int bh) {
+        const uint32_t slot = kv_it % L::kStages;
+        const uint32_t round = kv_it / L::kStages;
+        ok = mbar_wait_bounded(&bars.kv_empty[slot], (round & 1u) ^ 1u, abort_flag, &g_error_word,
+                               a.timeout_ns);
+        if (!ok) return;
+        mbar_arrive_expect_tx(&bars.kv_full[slot], L::kKVTileBytes);
+        uint8_t* dst = smem + L::kKVOff + slot * L::kKVTileBytes;
+#pragma unroll
+        for (int at = 0; at < L::kAtoms; ++at)
+            tma_load_3d_hint(dst + at * kTcBN * L::kAtomRowBytes, map, &bars.kv_full[slot],
+                             at * 64, j * kTcBN, bh, keep);
+        ++kv_it;
+    };
+
+    for (int t = blockIdx.x; t < a.num_tasks && ok; t += gridDim.x) {
+        const Task tk = decode_task<CAUSAL>(t, a);
+        load_q(0, tk);
+        if (!ok) break;
+        load_kv(&a.tmap_k, 0, tk.bh);
+        if (!ok) break;
+        if (tk.nb[1] > 0) {
+            load_q(1, tk);
+            if (!ok) break;
+        }
+        for (int j = 0; j < tk.nbmax && ok; ++j) {
+            load_kv(&a.tmap_v, j, tk.bh);
+            if (ok && j + 1 < tk.nbmax) load_kv(&a.tmap_k, j + 1, tk.bh);
+        }
+    }
+
+    // Drain: every bulk copy this thread started has landed before the CTA
+    // can retire (matters only when a wait gave up above).
+    for (uint32_t s = 0; s < (uint32_t)L::kStages && s < kv_it; ++s) {
+        const uint32_t last = s + ((kv_it - 1u - s) / L::kStages) * L::kStages;
+        mbar_wait_bounded(&bars.kv_full[s], (last / L::kStages) & 1u, nullptr, &g_error_word,
+                          a.timeout_ns);
+    }
+    for (int i = 0; i < 2; ++i)
+        if (qcnt[i] > 0u)
+            mbar_wait_bounded(&bars.q_full[i], (qcnt[i] - 1u) & 1u, nullptr, &g_error_word,
+                              a.timeout_ns);
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (one thread)
+// ---------------------------------------------------------------------------
+template <int D, bool BF16, bool CAUSAL>
+__device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint32_t tmem_base,
+                         volatile uint32_t* abort_flag) {
+    using L = TcLayout<D>;
+    constexpr uint32_t kIdescQK = idesc_f16_f32(kTcBM, kTcBN, BF16 ? 1u : 0u, 0u, 0u);
+    constexpr uint32_t kIdescPV = idesc_f16_f32(kTcBM, D, BF16 ? 1u : 0u, 0u, 1u);
+    const uint32_t q_smem = smem_u32(smem + L::kQOff);
+    const uint32_t kv_smem = smem_u32(smem + L::kKVOff);
+
+    uint32_t kv_it = 0;
+    uint32_t qcnt[2] = {0u, 0u};
+    uint32_t pcnt[2] = {0u, 0u};
+    bool ok = true;
+
+    auto wait_slot = [&](uint32_t& slot) {
+        slot = kv_it % L::kStages;
+        ok = mbar_wait_bounded(&bars.kv_full[slot], (kv_it / L::kStages) & 1u, abort_flag,
+                               &g_error_word, a.timeout_ns);
+        ++kv_it;
+        tc_fence_after();
+    };
+    // S_i = Q_i K^T : M=128 rows, N=128 keys, K=D in steps of 16 (32 bytes
+    // inside a 128-byte swizzle row; a new atom every 64 elements).
+    auto issue_qk = [&](int i, uint32_t kslot) {
+        const uint32_t qa = q_smem + i * L::kQTileBytes;
+        const uint32_t kb = kv_smem + kslot * L::kKVTileBytes;
+        const uint32_t d_tmem = tmem_base + i * kTcBN;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off_q = (kk / 4) * (kTcBM * 128) + (kk % 4) * 32;
+            const uint32_t off_k = (kk / 4) * (kTcBN * 128) + (kk % 4) * 32;
+            const uint64_t adesc = smem_desc_sw128(qa + off_q, 16, 1024);
+            const uint64_t bdesc = smem_desc_sw128(kb + off_k, 16, 1024);
+            mma_ss(d_tmem, adesc, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
+        }
+    };
+    // O_i (+)= P_i V : A = P_i from TMEM (8 columns per 16 keys), B = V tile,
+    // MN-major: 64-wide feature slabs of kTcBN rows x 128 bytes (leading
+    // offset = slab size), 8-key groups 1024 bytes apart (stride offset).
+    auto issue_pv = [&](int i, uint32_t vslot, bool accumulate) {
+        const uint32_t vb = kv_smem + vslot * L::kKVTileBytes;
+        const uint32_t d_tmem = tmem_base + 2 * kTcBN + i * D;
+        const uint32_t a_tmem = tmem_base + i * kTcBN;
+#pragma unroll
+        for (int kk = 0; kk < kTcBN / 16; ++kk) {
+            const uint64_t bdesc = smem_desc_sw128(vb + kk * 16 * 128, kTcBN * 128, 1024);
+            mma_ts(d_tmem, a_tmem + kk * 8, bdesc, kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+        }
+    };
+
+    for (int t = blockIdx.x; t < a.num_tasks && ok; t += gridDim.x) {
+        const Task tk = decode_task<CAUSAL>(t, a);
+        uint32_t kslot, vslot;
+        wait_slot(kslot);  // K_0
+        if (!ok) break;
+        for (int i = 0; i < 2 && ok; ++i) {
+            if (tk.nb[i] == 0) continue;
+            ok = mbar_wait_bounded(&bars.q_full[i], qcnt[i] & 1u, abort_flag, &g_error_word,
+                                   a.timeout_ns);
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk(i, kslot);
+            mma_commit(&bars.s_full[i]);
+            if (tk.nb[i] == 1) {
+                mma_commit(&bars.q_empty[i]);
+                ++qcnt[i];
+            }
+        }
+        if (!ok) break;
+        mma_commit(&bars.kv_empty[kslot]);
+
+        for (int j = 0; j < tk.nbmax && ok; ++j) {
+            const bool has_next = j + 1 < tk.nbmax;
+            wait_slot(vslot);  // V_j
+            if (!ok) break;
+            bool have_k = false;
+            for (int i = 0; i < 2; ++i) {
+                if (j < tk.nb[i]) {
+                    ok = mbar_wait_bounded(&bars.p_full[i], pcnt[i] & 1u, abort_flag,
+                                           &g_error_word, a.timeout_ns);
+                    ++pcnt[i];
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(i, vslot, j > 0);
+                    if (j == tk.nb[i] - 1) mma_commit(&bars.o_full[i]);
+                }
+                if (i == 1) mma_commit(&bars.kv_empty[vslot]);
+                if (has_next && !have_k) {
+                    wait_slot(kslot);  // K_{j+1}
+                    have_k = true;
+                    if (!ok) break;
+                }
+                if (j + 1 < tk.nb[i]) {
+                    issue_qk(i, kslot);
+                    mma_commit(&bars.s_full[i]);
+                    if (j + 1 == tk.nb[i] - 1) {
+                        mma_commit(&bars.q_empty[i]);
+                        ++qcnt[i];
+                    }
+                }
+            }
+            if (!ok) break;
+            if (has_next) mma_commit(&bars.kv_empty[kslot]);
+        }
+    }
+
+    // Drain: every MMA issued above has completed before TMEM is released.
+    mma_commit(bars.drain);
+    mbar_wait_bounded(bars.drain, 0u, nullptr, &g_error_word, a.timeout_ns);
+}
+
+// ---------------------------------------------------------------------------
+// Softmax + correction + epilogue (one warpgroup per Q tile)
+// ---------------------------------------------------------------------------
+template <int D, bool BF16, bool CAUSAL>
+__device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_base,
+                             volatile uint32_t* abort_flag) {
+    const int warp = threadIdx.x / 32;
+    const int tile = warp / 4;                  // which Q tile / S, P, O buffer
+    const int trow = threadIdx.x % kTcBM;       // row within the tile == TMEM lane
+    const uint32_t lane_field = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t tS = tmem_base + lane_field + tile * kTcBN;
+    const uint32_t tO = tmem_base + lane_field + 2 * kTcBN + tile * D;
+    const float sl2 = a.scale_log2;
+
+    uint32_t scnt = 0, ocnt = 0;
+    for (int t = blockIdx.x; t < a.num_tasks; t += gridDim.x) {
+        const Task tk = decode_task<CAUSAL>(t, a);
+        const int nb = tk.nb[tile];
+        if (nb == 0) continue;
+        const int row0 = tk.q0 + tile * kTcBM;
+        const int row = row0 + trow;
+        const int lim = CAUSAL ? min(row + 1, a.N) : a.N;  // keys < lim are visible to this row
+
+        float m_run = -INFINITY;  // running max of scale*log2(e)*s
+        float l_run = 0.f;        // running sum of exp2(scaled s - m_run)
+
+        for (int j = 0; j < nb; ++j) {
+            bool ok = mbar_wait_bounded(&bars.s_full[tile], scnt & 1u, abort_flag, &g_error_word,
+                                        a.timeout_ns);
+            ++scnt;
+            if (!__all_sync(0xffffffffu, ok)) return;
+            tc_fence_after();
+
+            // The whole score row: four 32-column loads in flight, one wait.
+            uint32_t sr[kTcBN / 32][32];
+#pragma unroll
+            for (int c = 0; c < kTcBN / 32; ++c) tmem_ld32(tS + c * 32, sr[c]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < kTcBN / 32; ++c) reg_fence(sr[c]);
+            float s[kTcBN];
+#pragma unroll
+            for (int c = 0; c < kTcBN; ++c) s[c] = __uint_as_float(sr[c / 32][c % 32]);
+
+            const int kb = j * kTcBN;
+            const bool need_mask = (kb + kTcBN > a.N) || (CAUSAL && kb + kTcBN - 1 > row0);
+            if (need_mask) {
+                const int vis = lim - kb;
+#pragma unroll
+                for (int c = 0; c < kTcBN; ++c)
+                    if (c >= vis) s[c] = -INFINITY;
+            }
+
+            float mx[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx[u] = s[u];
+#pragma unroll
+            for (int c = 8; c < kTcBN; ++c) mx[c % 8] = fmaxf(mx[c % 8], s[c]);
+            float mblk = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            const float m_new = fmaxf(m_run, mblk * sl2);
+
+            if (j == 0) {
+                m_run = m_new;
+            } else {
+                // Rescale O and l only when some row of the warp saw its max
+                // rise by more than the threshold; otherwise keep the stale
+                // max for P and l alike (exact in exact arithmetic, P <= 2^8).
+                const bool grow = (m_new - m_run) > kRescaleThreshold;
+                if (__any_sync(0xffffffffu, grow)) {
+                    const float alpha = ex2_approx(m_run - m_new);
+                    l_run *= alpha;
+                    m_run = m_new;
+                    uint32_t r[32];
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        tmem_ld32(tO + c * 32, r);
+                        tmem_wait_ld();
+                        reg_fence(r);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                        tmem_st32(tO + c * 32, r);
+                    }
+                }
+            }
+            const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
+
+            float ls[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+#pragma unroll
+            for (int c = 0; c < kTcBN / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * e], sl2, -m_sub));
+                    const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * e + 1], sl2, -m_sub));
+                    ls[e % 8] += p0 + p1;
+                    pk[e] = pack2(p0, p1, BF16);
+                }
+                tmem_st16(tS + c * 16, pk);
+            }
+            l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bars.p_full[tile]);
+        }
+
+        // Epilogue: O = O~ / l, LSE = (m + log2 l) ln 2, rows < N only.
+        bool ok = mbar_wait_bounded(&bars.o_full[tile], ocnt & 1u, abort_flag, &g_error_word,
+                                    a.timeout_ns);
+        ++ocnt;
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc_fence_after();
+        const float inv_l = 1.f / l_run;
+        const bool valid = row < a.N;
+        uint8_t* orow = reinterpret_cast<uint8_t*>(a.o) +
+                        ((static_cast<int64_t>(tk.bh) * a.N + row) * D) * 2;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tO + c * 32, r);
+            tmem_wait_ld();
+            reg_fence(r);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                pk[e] = pack2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l,
+                              BF16);
+            if (valid) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                    dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+            }
+        }
+        if (valid && a.lse != nullptr)
+            a.lse[static_cast<int64_t>(tk.bh) * a.N + row] = (m_run + log2f(l_run)) * kLn2;
+        tc_fence_before();
+    }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ TcArgs a) {
+    using L = TcLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const Bars bars = carve_bars<D>(smem);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+    volatile uint32_t* abort_flag = misc + 1;
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.q_full[i], 1);
+            mbar_init(&bars.q_empty[i], 1);
+            mbar_init(&bars.s_full[i], 1);
+            mbar_init(&bars.p_full[i], kTcBM);
+            mbar_init(&bars.o_full[i], 1);
+        }
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(&bars.kv_full[s], 1);
+            mbar_init(&bars.kv_empty[s], 1);
+        }
+        mbar_init(bars.drain, 1);
+        *abort_flag = 0u;
+        fence_barrier_init();
+    }
+    if (warp == 8) {
+        tmem_alloc(misc, L::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 9 && lane == 0) {
+        tma_prefetch_desc(&a.tmap_q);
+        tma_prefetch_desc(&a.tmap_k);
+        tma_prefetch_desc(&a.tmap_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = misc[0];
+
+    if (warp < 8) {
+        regs_increase<kSoftmaxRegs>();
+        softmax_role<D, BF16, CAUSAL>(a, bars, tmem_base, abort_flag);
+    } else {
+        regs_decrease<kControlRegs>();
+        if (warp == 8 && lane == 0)
+            mma_role<D, BF16, CAUSAL>(a, smem, bars, tmem_base, abort_flag);
+        else if (warp == 9 && lane == 0)
+            producer_role<D, CAUSAL>(a, smem, bars, abort_flag);
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, L::kTmemCols);
+    }
+}
+
+__global__ void wait_selftest_kernel(uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0u;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // Nothing ever arrives on `bar`: the bounded wait must give up, record
+    // the timeout in the error word and return.
+    if (threadIdx.x == 0)
+        (void)mbar_wait_bounded(&bar, 0u, &abort_flag, &g_error_word, timeout_ns);
+}
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_one(const TcArgs& a, int grid, cudaStream_t stream) {
+    using L = TcLayout<D>;
+    auto* fn = attn_fwd_tc_kernel<D, BF16, CAUSAL>;
+    // The opt-in above 48 KB of dynamic shared memory is per device: set it
+    // once for every device this instantiation is launched on.
+    static bool done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices || !done[dev]) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
+    }
+    fn<<<grid, kTcThreads, L::kAlloc, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_causal(const TcArgs& a, bool causal, int grid, cudaStream_t s) {
+    return causal ? launch_one<D, BF16, true>(a, grid, s) : launch_one<D, BF16, false>(a, grid, s);
+}
+
+}  // namespace
+
+int tc_smem_bytes(int D) { return D == 128 ? TcLayout<128>::kAlloc : TcLayout<64>::kAlloc; }
+int tc_num_stages(int D) { return D == 128 ? TcLayout<128>::kStages : TcLayout<64>::kStages; }
+
+cudaError_t tc_launch(const TcArgs& a, int D, bool bf16, bool causal, int grid,
+                      cudaStream_t stream) {
+    if (D == 128)
+        return bf16 ? launch_causal<128, true>(a, causal, grid, stream)
+                    : launch_causal<128, false>(a, causal, grid, stream);
+    return bf16 ? launch_causal<64, true>(a, causal, grid, stream)
+                : launch_causal<64, false>(a, causal, grid, stream);
+}
+
+cudaError_t read_and_clear_error_word(uint32_t* out) {
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v));
+    if (e != cudaSuccess) return e;
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+    *out = v;
+    return e;
+}
+
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace fattn

@@ -1,0 +1,53 @@
+// internal.h -- declarations shared by the translation units of libfattn.
+// Not part of the public ABI (see include/fattn.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fattn {
+
+constexpr int kMaxDevices = 64;
+
+// ---- tensor-core path (bf16 / fp16), fwd_tc.cu ------------------------------
+constexpr int kTcBM = 128;        // Q rows per MMA tile (tcgen05 M)
+constexpr int kTcQTiles = 2;      // Q tiles per task (rows per task = 256)
+constexpr int kTcBN = 128;        // keys per K/V tile (N of S = Q K^T)
+constexpr int kTcThreads = 384;   // 2 softmax warpgroups + 1 control warpgroup (MMA, TMA)
+
+struct TcArgs {
+    CUtensorMap tmap_q;  // 3-D {D, N, B*H}, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tmap_k;
+    CUtensorMap tmap_v;
+    void* o;             // [B,H,N,D] output, input dtype
+    float* lse;          // [B,H,N] or nullptr
+    int N;
+    int BH;
+    int num_qblk;        // ceil(N / 256)
+    int num_tasks;       // BH * num_qblk
+    float scale_log2;    // scale * log2(e)
+    uint64_t timeout_ns; // bound of every barrier wait
+};
+
+int tc_smem_bytes(int D);
+int tc_num_stages(int D);
+// Encodes the three tensor maps of `a` for these buffers (host).
+cudaError_t tc_encode_maps(TcArgs& a, const void* q, const void* k, const void* v, int64_t BH,
+                           int64_t N, int64_t D, bool bf16);
+cudaError_t tc_launch(const TcArgs& a, int D, bool bf16, bool causal, int grid,
+                      cudaStream_t stream);
+
+// ---- CUDA-core path (fp32), fwd_ffma.cu --------------------------------------
+constexpr int kFfmaBr = 128;      // Q rows per CTA = threads per CTA (one row per thread)
+int ffma_bc(int D);               // keys per K/V tile
+int ffma_smem_bytes(int D);
+cudaError_t ffma_launch(const float* q, const float* k, const float* v, float* o, float* lse,
+                        int64_t BH, int64_t N, int64_t D, float scale_log2, bool causal,
+                        cudaStream_t stream);
+
+// ---- device error word (fwd_tc.cu) -----------------------------------------
+cudaError_t read_and_clear_error_word(uint32_t* out);
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace fattn
