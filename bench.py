@@ -221,28 +221,11 @@ def run_ours(args, w, ws, rank, local):
     launches = args.steps  # fattn_fwd launches exactly one kernel per call
 
     # end to end through the host-buffer entry point
-    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
-    oh = torch.empty_like(q).pin_memory()
-    lh = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
-    e2e_steps = max(3, min(args.steps, 20))
-    for _ in range(2):
-        fattn.fwd_host(qh, kh, vh, qd, kd, vd, o, oh, lse, lh, causal=w.causal, scale=w.scale,
-                       stream=stream)
-    torch.cuda.synchronize(dev)
-    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    es.record(stream)
-    for _ in range(e2e_steps):
-        fattn.fwd_host(qh, kh, vh, qd, kd, vd, o, oh, lse, lh, causal=w.causal, scale=w.scale,
-                       stream=stream)
-    ee.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = es.elapsed_time(ee) / e2e_steps
-    elem = q.element_size()
-    h2d = 3 * q.numel() * elem
-    d2h = o.numel() * elem + lse.numel() * 4
-
+    e2e_ms, h2d, d2h = float("nan"), 0, 0
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = run_e2e(fattn, w, q, k, v, qd, kd, vd, o, lse, stream, dev, args.steps, barrier)
     times = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
+
     if ws > 1:
         import torch.distributed as dist
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
@@ -279,9 +262,10 @@ def run_ours(args, w, ws, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": DTYPE_NAMES[w.dtype], "data": "synthetic (seeded iid normal Q, K, V)",
         "config": config_of(w, ws), "pct_of_peak": 100.0 * roof["frac"], "roofline": roof,
-        "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms, "api": "fattn_fwd_host (pinned host buffers)"},
+        "e2e": ({"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                 "ms_per_step": e2e_ms, "api": "fattn_fwd_host (pinned host buffers)"}
+                if not args.no_e2e else None),
         "gpu_launches": launches, "clocks": clocks,
     }
     if not args.no_cpu_baseline:
@@ -293,6 +277,30 @@ def run_ours(args, w, ws, rank, local):
     if ws > 1:
         torch.distributed.destroy_process_group()
     return line
+
+
+def run_e2e(fattn, w, q, k, v, qd, kd, vd, o, lse, stream, dev, steps, barrier):
+    """Per step: H2D of Q, K, V from pinned memory, the kernel, D2H of O and LSE,
+    all enqueued by the library's host-buffer entry point."""
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty_like(q).pin_memory()
+    lh = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(steps, 20))
+    for _ in range(2):
+        fattn.fwd_host(qh, kh, vh, qd, kd, vd, o, oh, lse, lh, causal=w.causal, scale=w.scale,
+                       stream=stream)
+    torch.cuda.synchronize(dev)
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    es.record(stream)
+    for _ in range(e2e_steps):
+        fattn.fwd_host(qh, kh, vh, qd, kd, vd, o, oh, lse, lh, causal=w.causal, scale=w.scale,
+                       stream=stream)
+    ee.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = es.elapsed_time(ee) / e2e_steps
+    elem = q.element_size()
+    return e2e_ms, 3 * q.numel() * elem, o.numel() * elem + lse.numel() * 4
 
 
 def run_reference(args, w, ws, rank):
@@ -333,6 +341,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall time of the CPU oracle sample (cpu_baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

@@ -16,9 +16,9 @@
 //              (TMEM lane t): S row -> mask -> max -> exp2 -> P (16-bit) into
 //              TMEM, conditional O rescale, epilogue (O/l, LSE, store)
 //   warps 4-7  softmax warpgroup 1: same for Q tile 1
-//   warp 8     MMA issue (one thread): S_i = Q_i K_j^T (SS form),
+//   warp 8     MMA issue (one elected lane): S_i = Q_i K_j^T (SS form),
 //              O_i += P_i V_j (TS form), tcgen05.commit -> mbarriers
-//   warp 9     TMA producer (one thread): Q tiles once per task, K/V tiles
+//   warp 9     TMA producer (one elected lane): Q tiles once per task, K/V tiles
 //              through a ring of shared-memory stages
 //   warps 10-11 idle
 // The control warpgroup (warps 8-11) gives up registers (setmaxnreg) so the
@@ -65,8 +65,8 @@ struct TcLayout {
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = kTcQTiles * kQTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kKVTileBytes;
-    // q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] drain[1]
-    static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1;
+    // q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2][2] o_full[2] drain[1]
+    static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 4 + 2 + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kAlloc = kBytes + 1024;        // slack to align the base to 1024 B
@@ -121,7 +121,7 @@ struct Bars {
     uint64_t* kv_full;
     uint64_t* kv_empty;
     uint64_t* s_full;
-    uint64_t* p_full;
+    uint64_t* p_full;  // [tile * 2 + half]: first / second half of P_tile stored
     uint64_t* o_full;
     uint64_t* drain;
 };
@@ -137,7 +137,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
     r.kv_empty = r.kv_full + L::kStages;
     r.s_full = r.kv_empty + L::kStages;
     r.p_full = r.s_full + 2;
-    r.o_full = r.p_full + 2;
+    r.o_full = r.p_full + 4;
     r.drain = r.o_full + 2;
     return r;
 }
@@ -152,8 +152,16 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
     }
 }
 
+// Every lane of a warp waits; the outcome is made warp-uniform so that the
+// warp's control flow never diverges on a wait that gave up.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
+                                          volatile uint32_t* abort_flag, uint64_t timeout_ns) {
+    return __all_sync(0xffffffffu,
+                      mbar_wait_bounded(bar, parity, abort_flag, &g_error_word, timeout_ns));
+}
+
 // ---------------------------------------------------------------------------
-// TMA producer (one thread)
+// TMA producer (one warp; one elected lane issues the copies)
 // ---------------------------------------------------------------------------
 template <int D, bool CAUSAL>
 __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
@@ -166,29 +174,33 @@ __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
     const uint64_t once = l2_policy_evict_first();  // Q: read once
 
     auto load_q = [&](int i, const Task& tk) {
-        ok = mbar_wait_bounded(&bars.q_empty[i], (qcnt[i] & 1u) ^ 1u, abort_flag, &g_error_word,
-                               a.timeout_ns);
+        ok = warp_wait(&bars.q_empty[i], (qcnt[i] & 1u) ^ 1u, abort_flag, a.timeout_ns);
         if (!ok) return;
-        mbar_arrive_expect_tx(&bars.q_full[i], L::kQTileBytes);
-        uint8_t* dst = smem + L::kQOff + i * L::kQTileBytes;
+        if (elect_one_sync()) {
+            mbar_arrive_expect_tx(&bars.q_full[i], L::kQTileBytes);
+            uint8_t* dst = smem + L::kQOff + i * L::kQTileBytes;
 #pragma unroll
-        for (int at = 0; at < L::kAtoms; ++at)
-            tma_load_3d_hint(dst + at * kTcBM * L::kAtomRowBytes, &a.tmap_q, &bars.q_full[i],
-                             at * 64, tk.q0 + i * kTcBM, tk.bh, once);
+            for (int at = 0; at < L::kAtoms; ++at)
+                tma_load_3d_hint(dst + at * kTcBM * L::kAtomRowBytes, &a.tmap_q, &bars.q_full[i],
+                                 at * 64, tk.q0 + i * kTcBM, tk.bh, once);
+        }
+        __syncwarp();
         ++qcnt[i];
     };
     auto load_kv = [&](const CUtensorMap* map, int j, int bh) {
         const uint32_t slot = kv_it % L::kStages;
         const uint32_t round = kv_it / L::kStages;
-        ok = mbar_wait_bounded(&bars.kv_empty[slot], (round & 1u) ^ 1u, abort_flag, &g_error_word,
-                               a.timeout_ns);
+        ok = warp_wait(&bars.kv_empty[slot], (round & 1u) ^ 1u, abort_flag, a.timeout_ns);
         if (!ok) return;
-        mbar_arrive_expect_tx(&bars.kv_full[slot], L::kKVTileBytes);
-        uint8_t* dst = smem + L::kKVOff + slot * L::kKVTileBytes;
+        if (elect_one_sync()) {
+            mbar_arrive_expect_tx(&bars.kv_full[slot], L::kKVTileBytes);
+            uint8_t* dst = smem + L::kKVOff + slot * L::kKVTileBytes;
 #pragma unroll
-        for (int at = 0; at < L::kAtoms; ++at)
-            tma_load_3d_hint(dst + at * kTcBN * L::kAtomRowBytes, map, &bars.kv_full[slot],
-                             at * 64, j * kTcBN, bh, keep);
+            for (int at = 0; at < L::kAtoms; ++at)
+                tma_load_3d_hint(dst + at * kTcBN * L::kAtomRowBytes, map, &bars.kv_full[slot],
+                                 at * 64, j * kTcBN, bh, keep);
+        }
+        __syncwarp();
         ++kv_it;
     };
 
@@ -208,21 +220,18 @@ __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
         }
     }
 
-    // Drain: every bulk copy this thread started has landed before the CTA
-    // can retire (matters only when a wait gave up above).
+    // Drain: every bulk copy this warp started has landed before the CTA can
+    // retire (matters only when a wait gave up above).
     for (uint32_t s = 0; s < (uint32_t)L::kStages && s < kv_it; ++s) {
         const uint32_t last = s + ((kv_it - 1u - s) / L::kStages) * L::kStages;
-        mbar_wait_bounded(&bars.kv_full[s], (last / L::kStages) & 1u, nullptr, &g_error_word,
-                          a.timeout_ns);
+        warp_wait(&bars.kv_full[s], (last / L::kStages) & 1u, nullptr, a.timeout_ns);
     }
     for (int i = 0; i < 2; ++i)
-        if (qcnt[i] > 0u)
-            mbar_wait_bounded(&bars.q_full[i], (qcnt[i] - 1u) & 1u, nullptr, &g_error_word,
-                              a.timeout_ns);
+        if (qcnt[i] > 0u) warp_wait(&bars.q_full[i], (qcnt[i] - 1u) & 1u, nullptr, a.timeout_ns);
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (one thread)
+// MMA issuer (one warp; one elected lane issues MMAs and commits)
 // ---------------------------------------------------------------------------
 template <int D, bool BF16, bool CAUSAL>
 __device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint32_t tmem_base,
@@ -240,37 +249,46 @@ __device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint3
 
     auto wait_slot = [&](uint32_t& slot) {
         slot = kv_it % L::kStages;
-        ok = mbar_wait_bounded(&bars.kv_full[slot], (kv_it / L::kStages) & 1u, abort_flag,
-                               &g_error_word, a.timeout_ns);
+        ok = warp_wait(&bars.kv_full[slot], (kv_it / L::kStages) & 1u, abort_flag, a.timeout_ns);
         ++kv_it;
         tc_fence_after();
     };
+    // Descriptor templates with a zero start address.  A tile's descriptor is
+    // the template plus (shared address >> 4): the start-address field is the
+    // low 14 bits and every shared address is below 256 KB, so the add never
+    // carries.  Per-MMA steps are compile-time offsets on top, which keeps the
+    // issue loop to one 64-bit add per operand.
+    const uint64_t kmaj_desc = smem_desc_sw128(0u, 16u, 1024u);             // Q, K: K-major
+    const uint64_t vmn_desc = smem_desc_sw128(0u, kTcBN * 128u, 1024u);     // V: MN-major
     // S_i = Q_i K^T : M=128 rows, N=128 keys, K=D in steps of 16 (32 bytes
     // inside a 128-byte swizzle row; a new atom every 64 elements).
     auto issue_qk = [&](int i, uint32_t kslot) {
-        const uint32_t qa = q_smem + i * L::kQTileBytes;
-        const uint32_t kb = kv_smem + kslot * L::kKVTileBytes;
+        const uint64_t adesc = kmaj_desc + ((q_smem + i * L::kQTileBytes) >> 4);
+        const uint64_t bdesc = kmaj_desc + ((kv_smem + kslot * L::kKVTileBytes) >> 4);
         const uint32_t d_tmem = tmem_base + i * kTcBN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off_q = (kk / 4) * (kTcBM * 128) + (kk % 4) * 32;
-            const uint32_t off_k = (kk / 4) * (kTcBN * 128) + (kk % 4) * 32;
-            const uint64_t adesc = smem_desc_sw128(qa + off_q, 16, 1024);
-            const uint64_t bdesc = smem_desc_sw128(kb + off_k, 16, 1024);
-            mma_ss(d_tmem, adesc, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
+            constexpr uint32_t kAtomQ = kTcBM * 128, kAtomK = kTcBN * 128;
+            const uint64_t off_q = ((kk / 4) * kAtomQ + (kk % 4) * 32) >> 4;
+            const uint64_t off_k = ((kk / 4) * kAtomK + (kk % 4) * 32) >> 4;
+            mma_ss(d_tmem, adesc + off_q, bdesc + off_k, kIdescQK, kk > 0 ? 1u : 0u);
         }
     };
     // O_i (+)= P_i V : A = P_i from TMEM (8 columns per 16 keys), B = V tile,
     // MN-major: 64-wide feature slabs of kTcBN rows x 128 bytes (leading
     // offset = slab size), 8-key groups 1024 bytes apart (stride offset).
-    auto issue_pv = [&](int i, uint32_t vslot, bool accumulate) {
-        const uint32_t vb = kv_smem + vslot * L::kKVTileBytes;
+    // `half` selects keys [64*half, 64*half+64) of the tile (P columns
+    // [32*half, 32*half+32)), so the first half can run while the softmax
+    // warps still produce the second.
+    auto issue_pv = [&](int i, int half, uint32_t vslot, bool accumulate) {
+        const uint64_t bdesc = vmn_desc + ((kv_smem + vslot * L::kKVTileBytes) >> 4);
         const uint32_t d_tmem = tmem_base + 2 * kTcBN + i * D;
         const uint32_t a_tmem = tmem_base + i * kTcBN;
 #pragma unroll
-        for (int kk = 0; kk < kTcBN / 16; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(vb + kk * 16 * 128, kTcBN * 128, 1024);
-            mma_ts(d_tmem, a_tmem + kk * 8, bdesc, kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+        for (int k2 = 0; k2 < kTcBN / 32; ++k2) {
+            const int kk = half * (kTcBN / 32) + k2;
+            mma_ts(d_tmem, a_tmem + kk * 8, bdesc + ((kk * 16 * 128) >> 4), kIdescPV,
+                   (accumulate || kk > 0) ? 1u : 0u);
         }
     };
 
@@ -281,19 +299,20 @@ __device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint3
         if (!ok) break;
         for (int i = 0; i < 2 && ok; ++i) {
             if (tk.nb[i] == 0) continue;
-            ok = mbar_wait_bounded(&bars.q_full[i], qcnt[i] & 1u, abort_flag, &g_error_word,
-                                   a.timeout_ns);
+            ok = warp_wait(&bars.q_full[i], qcnt[i] & 1u, abort_flag, a.timeout_ns);
             if (!ok) break;
             tc_fence_after();
-            issue_qk(i, kslot);
-            mma_commit(&bars.s_full[i]);
-            if (tk.nb[i] == 1) {
-                mma_commit(&bars.q_empty[i]);
-                ++qcnt[i];
+            if (elect_one_sync()) {
+                issue_qk(i, kslot);
+                mma_commit(&bars.s_full[i]);
+                if (tk.nb[i] == 1) mma_commit(&bars.q_empty[i]);
             }
+            __syncwarp();
+            if (tk.nb[i] == 1) ++qcnt[i];
         }
         if (!ok) break;
-        mma_commit(&bars.kv_empty[kslot]);
+        if (elect_one_sync()) mma_commit(&bars.kv_empty[kslot]);
+        __syncwarp();
 
         for (int j = 0; j < tk.nbmax && ok; ++j) {
             const bool has_next = j + 1 < tk.nbmax;
@@ -302,37 +321,51 @@ __device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint3
             bool have_k = false;
             for (int i = 0; i < 2; ++i) {
                 if (j < tk.nb[i]) {
-                    ok = mbar_wait_bounded(&bars.p_full[i], pcnt[i] & 1u, abort_flag,
-                                           &g_error_word, a.timeout_ns);
+                    for (int half = 0; half < 2 && ok; ++half) {
+                        ok = warp_wait(&bars.p_full[2 * i + half], pcnt[i] & 1u, abort_flag,
+                                       a.timeout_ns);
+                        if (!ok) break;
+                        tc_fence_after();
+                        if (elect_one_sync()) {
+                            issue_pv(i, half, vslot, j > 0);
+                            if (half == 1 && j == tk.nb[i] - 1) mma_commit(&bars.o_full[i]);
+                        }
+                        __syncwarp();
+                    }
                     ++pcnt[i];
                     if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(i, vslot, j > 0);
-                    if (j == tk.nb[i] - 1) mma_commit(&bars.o_full[i]);
                 }
-                if (i == 1) mma_commit(&bars.kv_empty[vslot]);
+                if (i == 1) {
+                    if (elect_one_sync()) mma_commit(&bars.kv_empty[vslot]);
+                    __syncwarp();
+                }
                 if (has_next && !have_k) {
                     wait_slot(kslot);  // K_{j+1}
                     have_k = true;
                     if (!ok) break;
                 }
                 if (j + 1 < tk.nb[i]) {
-                    issue_qk(i, kslot);
-                    mma_commit(&bars.s_full[i]);
-                    if (j + 1 == tk.nb[i] - 1) {
-                        mma_commit(&bars.q_empty[i]);
-                        ++qcnt[i];
+                    if (elect_one_sync()) {
+                        issue_qk(i, kslot);
+                        mma_commit(&bars.s_full[i]);
+                        if (j + 1 == tk.nb[i] - 1) mma_commit(&bars.q_empty[i]);
                     }
+                    __syncwarp();
+                    if (j + 1 == tk.nb[i] - 1) ++qcnt[i];
                 }
             }
             if (!ok) break;
-            if (has_next) mma_commit(&bars.kv_empty[kslot]);
+            if (has_next) {
+                if (elect_one_sync()) mma_commit(&bars.kv_empty[kslot]);
+                __syncwarp();
+            }
         }
     }
 
     // Drain: every MMA issued above has completed before TMEM is released.
-    mma_commit(bars.drain);
-    mbar_wait_bounded(bars.drain, 0u, nullptr, &g_error_word, a.timeout_ns);
+    if (elect_one_sync()) mma_commit(bars.drain);
+    __syncwarp();
+    warp_wait(bars.drain, 0u, nullptr, a.timeout_ns);
 }
 
 // ---------------------------------------------------------------------------
@@ -359,13 +392,13 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
         const int lim = CAUSAL ? min(row + 1, a.N) : a.N;  // keys < lim are visible to this row
 
         float m_run = -INFINITY;  // running max of scale*log2(e)*s
-        float l_run = 0.f;        // running sum of exp2(scaled s - m_run)
+        float l_run = 0.f;        // running sum of the 16-bit P values fed to the MMA (normalises O)
+        float l_exact = 0.f;      // running sum of the unrounded P values (gives the LSE)
 
         for (int j = 0; j < nb; ++j) {
-            bool ok = mbar_wait_bounded(&bars.s_full[tile], scnt & 1u, abort_flag, &g_error_word,
-                                        a.timeout_ns);
+            const bool ok = warp_wait(&bars.s_full[tile], scnt & 1u, abort_flag, a.timeout_ns);
             ++scnt;
-            if (!__all_sync(0xffffffffu, ok)) return;
+            if (!ok) return;
             tc_fence_after();
 
             // The whole score row: four 32-column loads in flight, one wait.
@@ -388,13 +421,14 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
                     if (c >= vis) s[c] = -INFINITY;
             }
 
+            // Row max: eight independent chains of three-input max.
             float mx[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) mx[u] = s[u];
 #pragma unroll
-            for (int c = 8; c < kTcBN; ++c) mx[c % 8] = fmaxf(mx[c % 8], s[c]);
-            float mblk = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            for (int c = 8; c < kTcBN; c += 2) mx[(c / 2) % 8] = fmax3f(mx[(c / 2) % 8], s[c], s[c + 1]);
+            const float mblk = fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]),
+                                      fmaxf(mx[6], mx[7]));
             const float m_new = fmaxf(m_run, mblk * sl2);
 
             if (j == 0) {
@@ -407,6 +441,7 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
                 if (__any_sync(0xffffffffu, grow)) {
                     const float alpha = ex2_approx(m_run - m_new);
                     l_run *= alpha;
+                    l_exact *= alpha;
                     m_run = m_new;
                     uint32_t r[32];
 #pragma unroll
@@ -421,34 +456,48 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
                     }
                 }
             }
-            const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
+            const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
 
-            float ls[8];
+            // P = exp2(s*scale*log2e - m) rounded to the operand type, written
+            // over the first half of S.  l_run sums exactly the rounded values
+            // the P.V product consumes, so O is normalised by the weights it
+            // was built from; l_exact sums the unrounded ones for the LSE.
+            float la[8], le[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+            for (int u = 0; u < 8; ++u) {
+                la[u] = 0.f;
+                le[u] = 0.f;
+            }
 #pragma unroll
             for (int c = 0; c < kTcBN / 32; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * e], sl2, -m_sub));
-                    const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * e + 1], sl2, -m_sub));
-                    ls[e % 8] += p0 + p1;
+                    float x0, x1;
+                    ffma2(x0, x1, s[c * 32 + 2 * e], s[c * 32 + 2 * e + 1], sl2, sl2, neg_m, neg_m);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                     pk[e] = pack2(p0, p1, BF16);
+                    add_packed16_to_f32<BF16>(la[(e % 4) * 2], la[(e % 4) * 2 + 1], pk[e]);
+                    fadd2(le[(e % 4) * 2], le[(e % 4) * 2 + 1], p0, p1);
                 }
                 tmem_st16(tS + c * 16, pk);
+                if (c % 2 == 1) {
+                    // Half of P stored: hand it to the MMA warp (one arrival
+                    // per warp, after every lane's stores have completed).
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if ((threadIdx.x % 32) == 0) mbar_arrive(&bars.p_full[2 * tile + c / 2]);
+                }
             }
-            l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&bars.p_full[tile]);
+            l_run += ((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7]));
+            l_exact += ((le[0] + le[1]) + (le[2] + le[3])) + ((le[4] + le[5]) + (le[6] + le[7]));
         }
 
         // Epilogue: O = O~ / l, LSE = (m + log2 l) ln 2, rows < N only.
-        bool ok = mbar_wait_bounded(&bars.o_full[tile], ocnt & 1u, abort_flag, &g_error_word,
-                                    a.timeout_ns);
+        const bool ok = warp_wait(&bars.o_full[tile], ocnt & 1u, abort_flag, a.timeout_ns);
         ++ocnt;
-        if (!__all_sync(0xffffffffu, ok)) return;
+        if (!ok) return;
         tc_fence_after();
         const float inv_l = 1.f / l_run;
         const bool valid = row < a.N;
@@ -473,7 +522,7 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
             }
         }
         if (valid && a.lse != nullptr)
-            a.lse[static_cast<int64_t>(tk.bh) * a.N + row] = (m_run + log2f(l_run)) * kLn2;
+            a.lse[static_cast<int64_t>(tk.bh) * a.N + row] = (m_run + log2f(l_exact)) * kLn2;
         tc_fence_before();
     }
 }
@@ -495,7 +544,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid
             mbar_init(&bars.q_full[i], 1);
             mbar_init(&bars.q_empty[i], 1);
             mbar_init(&bars.s_full[i], 1);
-            mbar_init(&bars.p_full[i], kTcBM);
+            mbar_init(&bars.p_full[2 * i], kTcBM / 32);  // one arrival per softmax warp
+            mbar_init(&bars.p_full[2 * i + 1], kTcBM / 32);
             mbar_init(&bars.o_full[i], 1);
         }
         for (int s = 0; s < L::kStages; ++s) {
@@ -525,9 +575,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid
         softmax_role<D, BF16, CAUSAL>(a, bars, tmem_base, abort_flag);
     } else {
         regs_decrease<kControlRegs>();
-        if (warp == 8 && lane == 0)
+        if (warp == 8)
             mma_role<D, BF16, CAUSAL>(a, smem, bars, tmem_base, abort_flag);
-        else if (warp == 9 && lane == 0)
+        else if (warp == 9)
             producer_role<D, CAUSAL>(a, smem, bars, abort_flag);
     }
     __syncwarp();

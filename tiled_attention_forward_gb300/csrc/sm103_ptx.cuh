@@ -50,6 +50,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// Test for completion of the phase with the given parity (the thread may be
+// suspended for a short, system-defined time while it is incomplete).  No
+// explicit suspend-time hint: a long hint was measured to delay the wake-up
+// of a waiting warp by a few hundred cycles.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -75,16 +79,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
                                                   uint32_t* err_word, uint64_t timeout_ns) {
     const uint32_t addr = smem_u32(bar);
     if (mbar_try_wait(addr, parity)) return true;
-    uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
         if (mbar_try_wait(addr, parity)) return true;
-        if ((it & 63u) == 0u) {
-            if (abort_flag != nullptr && *abort_flag != 0u) return false;
-            if (globaltimer_ns() - t0 > timeout_ns) {
-                atomicOr(err_word, 1u << kDevErrTimeout);
-                if (abort_flag != nullptr) *abort_flag = 1u;
-                return false;
-            }
+        if (abort_flag != nullptr && *abort_flag != 0u) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            atomicOr(err_word, 1u << kDevErrTimeout);
+            if (abort_flag != nullptr) *abort_flag = 1u;
+            return false;
         }
     }
 }
@@ -293,6 +295,66 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, uin
            | (b_mn << 16)            // B major
            | ((N >> 3) << 17)        // N / 8
            | ((M >> 4) << 24);       // M / 16
+}
+
+// One lane of the (converged) warp is elected; the same lane every time the
+// full warp executes this.
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .b32 rx;\n\t.reg .pred px;\n\t"
+        "elect.sync rx|px, %1;\n\t"
+        "@px mov.s32 %0, 1;\n\t}"
+        : "+r"(pred)
+        : "r"(0xFFFFFFFFu));
+    return pred != 0u;
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1), one packed fp32 instruction.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                      float c0, float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// (d0, d1) += (a0, a1), one packed fp32 instruction.
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) {
+    asm("{\n\t.reg .b64 ra, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rd, {%0, %1};\n\t"
+        "add.rn.f32x2 rd, rd, ra;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1));
+}
+
+// acc_lo += low 16-bit value of `packed`, acc_hi += high one (exact widening
+// of bf16 / fp16 to fp32 inside the add).
+template <bool BF16>
+__device__ __forceinline__ void add_packed16_to_f32(float& acc_lo, float& acc_hi, uint32_t packed) {
+    if (BF16)
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+            : "+f"(acc_lo), "+f"(acc_hi)
+            : "r"(packed));
+    else
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+            : "+f"(acc_lo), "+f"(acc_hi)
+            : "r"(packed));
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
