@@ -42,6 +42,34 @@ if ROOT not in sys.path:
 from tiled_attention_forward_gb300.inputs import BY_NAME, HEADLINE, workload_inputs  # noqa: E402
 
 METRIC = "attn fwd TFLOP/s (B=4,H=16,N=4096,D=128 bf16) and % of GB300 BF16 peak"
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the kernel on each workload, from an ncu capture (summaries under profiles/),
+# tagged with the hash of the kernel sources it was taken on.  Reported only
+# while the sources still hash the same; null once the kernel has changed.
+KERNEL_SOURCES = ["fwd_tc.cu", "fwd_ffma.cu", "sm103_ptx.cuh", "internal.h", "fattn_api.cu"]
+NCU_TRAFFIC = {
+    "bf16_B4_H16_N4096_D128": (201609472 + 37907712, "2a19fa906990269c"),
+    "fp16_B1_H16_N16000_D64_causal": (125040128 + 15502080, "2a19fa906990269c"),
+    "fp32_B4_H8_N8192_D64_causal": (202531584 + 52426752, "2a19fa906990269c"),
+}
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tiled_attention_forward_gb300", "csrc")
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    entry = NCU_TRAFFIC.get(workload)
+    if entry is None or entry[1] != kernel_source_hash():
+        return None
+    return entry[0]
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
@@ -62,6 +90,27 @@ def load_peaks():
             p = json.load(f)
         return p, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank timings (a no-op without a process group)."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_tflops(flops_per_step, n_ranks, steps, ms_total_max):
+    """Work of every rank (weak scaling: each rank runs the full workload) over
+    the slowest rank's time."""
+    return flops_per_step * n_ranks * steps / (ms_total_max * 1e-3) / 1e12
+
+
+def w_bytes(w):
+    """Compulsory HBM bytes of one forward: read Q, K, V once, write O and LSE once."""
+    e = {"fp32": 4, "fp16": 2, "bf16": 2}[w.dtype]
+    return 4 * w.B * w.H * w.N * w.D * e + 4 * w.B * w.H * w.N
 
 
 def config_of(w, n_gpus):
@@ -224,12 +273,7 @@ def run_ours(args, w, ws, rank, local):
     e2e_ms, h2d, d2h = float("nan"), 0, 0
     if not args.no_e2e:
         e2e_ms, h2d, d2h = run_e2e(fattn, w, q, k, v, qd, kd, vd, o, lse, stream, dev, args.steps, barrier)
-    times = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
-
-    if ws > 1:
-        import torch.distributed as dist
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms_total, e2e_ms = times.tolist()
+    ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], device=dev)
     clocks = sampler.summary(t0, t1)
     if rank != 0:
         if ws > 1:
@@ -238,7 +282,7 @@ def run_ours(args, w, ws, rank, local):
 
     flops = w.flops()
     ms_per_step = ms_total / args.steps
-    value = flops * ws * args.steps / (ms_total * 1e-3) / 1e12
+    value = whole_job_tflops(flops, ws, args.steps, ms_total)
     achieved = flops / (ms_per_step * 1e-3) / 1e12  # one launch = one step on this GPU
     peaks, peak_src = load_peaks()
     peak_key = "bf16_tflops"
@@ -246,16 +290,17 @@ def run_ours(args, w, ws, rank, local):
         sm_mhz = peaks.get("sm_max_mhz", 2070.0)
         peak = torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT,
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": ncu_traffic(w.name),
                 "peak_source": "FP32 FFMA: SMs x 128 lanes x 2 FLOP x max SM clock (%s clock)" % peak_src}
     else:
         peak = float(peaks[peak_key])
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": ncu_traffic(w.name),
                 "peak_source": "%s dense bf16 (cuBLAS burst) of %s; fp16 taken at the same rate"
                                % (peak_key, peak_src),
                 "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak))}
-    roof["traffic_note"] = "DRAM bytes per launch from ncu: see profiles/"
+    roof["traffic_note"] = ("DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum); "
+                            "algorithmic compulsory bytes (Q+K+V read, O+LSE write): %d" % w_bytes(w))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_median": statistics.median(per),
