@@ -70,7 +70,9 @@ typedef enum {
     FATTN_ERR_MISALIGNED = 3,    /* a tensor pointer not 16-byte aligned (TMA / vector access requirement) */
     FATTN_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (launch, copy, tensor-map encode) */
     FATTN_ERR_TIMEOUT = 5,       /* a kernel's bounded wait expired (reported by fattn_get_device_status) */
-    FATTN_ERR_NO_DEVICE = 6      /* no usable sm_103 device is current */
+    FATTN_ERR_NO_DEVICE = 6,     /* no usable sm_103 device is current */
+    FATTN_ERR_INTERNAL = 7       /* a kernel found a broken launch invariant and did no work
+                                    (reported by fattn_get_device_status) */
 } fattn_status;
 
 /*
@@ -131,8 +133,10 @@ FATTN_API int fattn_plan(int64_t B, int64_t H, int64_t N, int64_t D, int causal,
 /*
  * fattn_get_device_status -- synchronises `stream`, then reads and clears the
  * current device's error word.  Returns FATTN_OK, FATTN_ERR_TIMEOUT if a
- * kernel gave up a bounded wait since the last call, or FATTN_ERR_CUDA if the
- * synchronisation itself failed.
+ * kernel gave up a bounded wait since the last call, FATTN_ERR_INTERNAL if a
+ * kernel found a broken launch invariant (e.g. shared-memory alignment) and
+ * returned without computing, or FATTN_ERR_CUDA if the synchronisation itself
+ * failed.
  */
 FATTN_API int fattn_get_device_status(fattn_stream_t stream);
 

@@ -28,7 +28,7 @@ _LIB_PATH = os.path.join(_HERE, "libfattn.so")
 DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 STATUS = {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPORTED",
           3: "FATTN_ERR_MISALIGNED", 4: "FATTN_ERR_CUDA", 5: "FATTN_ERR_TIMEOUT",
-          6: "FATTN_ERR_NO_DEVICE"}
+          6: "FATTN_ERR_NO_DEVICE", 7: "FATTN_ERR_INTERNAL"}
 PLAN_FIELDS = ("path", "grid_x", "grid_y", "threads", "smem_bytes", "tasks", "kv_tiles",
                "rows_per_task", "keys_per_kv_tile")
 

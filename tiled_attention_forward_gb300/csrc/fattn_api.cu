@@ -137,6 +137,7 @@ const char* fattn_status_string(int status) {
         case FATTN_ERR_CUDA: return "FATTN_ERR_CUDA";
         case FATTN_ERR_TIMEOUT: return "FATTN_ERR_TIMEOUT";
         case FATTN_ERR_NO_DEVICE: return "FATTN_ERR_NO_DEVICE";
+        case FATTN_ERR_INTERNAL: return "FATTN_ERR_INTERNAL";
         default: return "FATTN_ERR_UNKNOWN";
     }
 }
@@ -264,6 +265,7 @@ int fattn_get_device_status(fattn_stream_t stream_h) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FATTN_ERR_CUDA;
     uint32_t word = 0;
     if (read_and_clear_error_word(&word) != cudaSuccess) return FATTN_ERR_CUDA;
+    if (word & (1u << FATTN_ERR_INTERNAL)) return FATTN_ERR_INTERNAL;
     if (word & (1u << FATTN_ERR_TIMEOUT)) return FATTN_ERR_TIMEOUT;
     return FATTN_OK;
 }

@@ -65,13 +65,16 @@ struct TcLayout {
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = kTcQTiles * kQTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kKVTileBytes;
-    // q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2][2] o_full[2] drain[1]
-    static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 4 + 2 + 1;
+    // q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] drain[1]
+    static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kBytes = kMiscOff + 16;
-    static constexpr int kAlloc = kBytes + 1024;        // slack to align the base to 1024 B
+    static constexpr int kAlloc = kBytes;  // the dynamic base is declared 1024-byte aligned
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+    // The MMA warp holds two ring slots (V_j, K_{j+1}) until the end of an
+    // iteration and then needs V_{j+1} and K_{j+2}: four slots at least.
+    static_assert(kStages >= 4, "K/V ring depth");
     static_assert(256 + 2 * D <= 512, "TMEM budget");
 };
 
@@ -121,7 +124,7 @@ struct Bars {
     uint64_t* kv_full;
     uint64_t* kv_empty;
     uint64_t* s_full;
-    uint64_t* p_full;  // [tile * 2 + half]: first / second half of P_tile stored
+    uint64_t* p_full;  // [tile]: P_tile stored (and O_tile rescaled)
     uint64_t* o_full;
     uint64_t* drain;
 };
@@ -137,7 +140,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
     r.kv_empty = r.kv_full + L::kStages;
     r.s_full = r.kv_empty + L::kStages;
     r.p_full = r.s_full + 2;
-    r.o_full = r.p_full + 4;
+    r.o_full = r.p_full + 2;
     r.drain = r.o_full + 2;
     return r;
 }
@@ -277,19 +280,14 @@ __device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint3
     // O_i (+)= P_i V : A = P_i from TMEM (8 columns per 16 keys), B = V tile,
     // MN-major: 64-wide feature slabs of kTcBN rows x 128 bytes (leading
     // offset = slab size), 8-key groups 1024 bytes apart (stride offset).
-    // `half` selects keys [64*half, 64*half+64) of the tile (P columns
-    // [32*half, 32*half+32)), so the first half can run while the softmax
-    // warps still produce the second.
-    auto issue_pv = [&](int i, int half, uint32_t vslot, bool accumulate) {
+    auto issue_pv = [&](int i, uint32_t vslot, bool accumulate) {
         const uint64_t bdesc = vmn_desc + ((kv_smem + vslot * L::kKVTileBytes) >> 4);
         const uint32_t d_tmem = tmem_base + 2 * kTcBN + i * D;
         const uint32_t a_tmem = tmem_base + i * kTcBN;
 #pragma unroll
-        for (int k2 = 0; k2 < kTcBN / 32; ++k2) {
-            const int kk = half * (kTcBN / 32) + k2;
+        for (int kk = 0; kk < kTcBN / 16; ++kk)
             mma_ts(d_tmem, a_tmem + kk * 8, bdesc + ((kk * 16 * 128) >> 4), kIdescPV,
                    (accumulate || kk > 0) ? 1u : 0u);
-        }
     };
 
     for (int t = blockIdx.x; t < a.num_tasks && ok; t += gridDim.x) {
@@ -314,34 +312,28 @@ __device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint3
         if (elect_one_sync()) mma_commit(&bars.kv_empty[kslot]);
         __syncwarp();
 
+        // Per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).  A commit costs
+        // the tensor pipe a drain, and adjacent commits drain once, so every
+        // signal except "S_0 ready" is committed together at the end of the
+        // iteration.
         for (int j = 0; j < tk.nbmax && ok; ++j) {
             const bool has_next = j + 1 < tk.nbmax;
             wait_slot(vslot);  // V_j
             if (!ok) break;
-            bool have_k = false;
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < 2 && ok; ++i) {
                 if (j < tk.nb[i]) {
-                    for (int half = 0; half < 2 && ok; ++half) {
-                        ok = warp_wait(&bars.p_full[2 * i + half], pcnt[i] & 1u, abort_flag,
-                                       a.timeout_ns);
-                        if (!ok) break;
-                        tc_fence_after();
-                        if (elect_one_sync()) {
-                            issue_pv(i, half, vslot, j > 0);
-                            if (half == 1 && j == tk.nb[i] - 1) mma_commit(&bars.o_full[i]);
-                        }
-                        __syncwarp();
-                    }
+                    ok = warp_wait(&bars.p_full[i], pcnt[i] & 1u, abort_flag, a.timeout_ns);
                     ++pcnt[i];
                     if (!ok) break;
-                }
-                if (i == 1) {
-                    if (elect_one_sync()) mma_commit(&bars.kv_empty[vslot]);
+                    tc_fence_after();
+                    if (elect_one_sync()) {
+                        issue_pv(i, vslot, j > 0);
+                        if (j == tk.nb[i] - 1) mma_commit(&bars.o_full[i]);
+                    }
                     __syncwarp();
                 }
-                if (has_next && !have_k) {
+                if (i == 0 && has_next) {
                     wait_slot(kslot);  // K_{j+1}
-                    have_k = true;
                     if (!ok) break;
                 }
                 if (j + 1 < tk.nb[i]) {
@@ -355,10 +347,12 @@ __device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint3
                 }
             }
             if (!ok) break;
-            if (has_next) {
-                if (elect_one_sync()) mma_commit(&bars.kv_empty[kslot]);
-                __syncwarp();
+            // V_j and K_{j+1} are released once every MMA issued so far is done.
+            if (elect_one_sync()) {
+                mma_commit(&bars.kv_empty[vslot]);
+                if (has_next) mma_commit(&bars.kv_empty[kslot]);
             }
+            __syncwarp();
         }
     }
 
@@ -481,15 +475,13 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
                     fadd2(le[(e % 4) * 2], le[(e % 4) * 2 + 1], p0, p1);
                 }
                 tmem_st16(tS + c * 16, pk);
-                if (c % 2 == 1) {
-                    // Half of P stored: hand it to the MMA warp (one arrival
-                    // per warp, after every lane's stores have completed).
-                    tmem_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if ((threadIdx.x % 32) == 0) mbar_arrive(&bars.p_full[2 * tile + c / 2]);
-                }
             }
+            // P stored: hand it to the MMA warp (one arrival per warp, after
+            // every lane's stores have completed).
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if ((threadIdx.x % 32) == 0) mbar_arrive(&bars.p_full[tile]);
             l_run += ((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7]));
             l_exact += ((le[0] + le[1]) + (le[2] + le[3])) + ((le[4] + le[5]) + (le[6] + le[7]));
         }
@@ -530,9 +522,15 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ TcArgs a) {
     using L = TcLayout<D>;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    // 128-byte-swizzled TMA destinations and MMA operands need 1024-byte
+    // aligned tiles.  Should the runtime ever place the dynamic window
+    // differently, report it and leave before touching anything.
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if ((smem_u32(smem_raw) & 1023u) != 0u) {
+        if (threadIdx.x == 0) atomicOr(&g_error_word, 1u << kDevErrInternal);
+        return;
+    }
+    uint8_t* smem = smem_raw;
     const Bars bars = carve_bars<D>(smem);
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile uint32_t* abort_flag = misc + 1;
@@ -544,8 +542,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid
             mbar_init(&bars.q_full[i], 1);
             mbar_init(&bars.q_empty[i], 1);
             mbar_init(&bars.s_full[i], 1);
-            mbar_init(&bars.p_full[2 * i], kTcBM / 32);  // one arrival per softmax warp
-            mbar_init(&bars.p_full[2 * i + 1], kTcBM / 32);
+            mbar_init(&bars.p_full[i], kTcBM / 32);  // one arrival per softmax warp
             mbar_init(&bars.o_full[i], 1);
         }
         for (int s = 0; s < L::kStages; ++s) {

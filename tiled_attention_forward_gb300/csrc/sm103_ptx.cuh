@@ -11,8 +11,9 @@
 
 namespace fattn {
 
-// Error word values written by kernels (mirrors fattn_status codes).
+// Error word bits written by kernels (bit k = fattn_status code k).
 constexpr uint32_t kDevErrTimeout = 5u;
+constexpr uint32_t kDevErrInternal = 7u;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
