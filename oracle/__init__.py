@@ -49,9 +49,14 @@ class OracleLib:
                                           ctypes.c_double, ci, dp]
         lib.attn_oracle_online_fwd.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64, i64,
                                                ctypes.c_double, ci, i64, i64, ci]
+        lib.attn_oracle_fwd_gqa.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64, i64, i64,
+                                            ctypes.c_double, ci, ci]
+        lib.attn_oracle_rows_gqa.argtypes = [dp, dp, dp, i64, i64, i64, i64, i64,
+                                             ctypes.c_double, ci, i64p, i64p, i64, dp, dp, ci]
         lib.attn_oracle_default_threads.argtypes = []
         for f in ("attn_oracle_fwd", "attn_oracle_rows", "attn_oracle_probs",
-                  "attn_oracle_online_fwd", "attn_oracle_default_threads"):
+                  "attn_oracle_online_fwd", "attn_oracle_fwd_gqa", "attn_oracle_rows_gqa",
+                  "attn_oracle_default_threads"):
             getattr(lib, f).restype = ci
         self._lib = lib
         self.path = path
@@ -70,6 +75,42 @@ class OracleLib:
                                        int(nthreads))
         if rc != 0:
             raise RuntimeError("attn_oracle_fwd failed: %d" % rc)
+        return o, lse
+
+    def attention_gqa(self, q, k, v, scale, causal=False, nthreads=0):
+        """Grouped-query forward: q [B,H,N,D], k and v [B,Hkv,N,D], H % Hkv == 0."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        if q.ndim != 4 or k.shape != v.shape or k.ndim != 4:
+            raise ValueError("q [B,H,N,D], k and v [B,Hkv,N,D]")
+        B, H, N, D = q.shape
+        if k.shape[0] != B or k.shape[2] != N or k.shape[3] != D:
+            raise ValueError("k/v must match q in B, N and D")
+        Hkv = k.shape[1]
+        o = np.empty((B, H, N, D), np.float64)
+        lse = np.empty((B, H, N), np.float64)
+        rc = self._lib.attn_oracle_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                           B, H, Hkv, N, D, float(scale), int(bool(causal)),
+                                           int(nthreads))
+        if rc != 0:
+            raise RuntimeError("attn_oracle_fwd_gqa failed: %d" % rc)
+        return o, lse
+
+    def attention_rows_gqa(self, q, k, v, scale, causal, bh_idx, row_idx, nthreads=0):
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, H, N, D = q.shape
+        Hkv = k.shape[1]
+        bh = np.ascontiguousarray(np.asarray(bh_idx, dtype=np.int64))
+        ri = np.ascontiguousarray(np.asarray(row_idx, dtype=np.int64))
+        R = bh.shape[0]
+        o = np.empty((R, D), np.float64)
+        lse = np.empty((R,), np.float64)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        rc = self._lib.attn_oracle_rows_gqa(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, N, D,
+                                            float(scale), int(bool(causal)),
+                                            bh.ctypes.data_as(i64p), ri.ctypes.data_as(i64p), R,
+                                            _ptr(o), _ptr(lse), int(nthreads))
+        if rc != 0:
+            raise RuntimeError("attn_oracle_rows_gqa failed: %d" % rc)
         return o, lse
 
     def attention_rows(self, q, k, v, scale, causal, bh_idx, row_idx, nthreads=0):
@@ -145,6 +186,14 @@ def probabilities(q, k, scale, causal=False, bh=0):
     return _get().probabilities(q, k, scale, causal, bh)
 
 
+def attention_gqa(q, k, v, scale, causal=False, nthreads=0):
+    return _get().attention_gqa(q, k, v, scale, causal, nthreads)
+
+
+def attention_rows_gqa(q, k, v, scale, causal, bh_idx, row_idx, nthreads=0):
+    return _get().attention_rows_gqa(q, k, v, scale, causal, bh_idx, row_idx, nthreads)
+
+
 def attention_online(q, k, v, scale, causal=False, Br=128, Bc=32, nthreads=0):
     return _get().attention_online(q, k, v, scale, causal, Br, Bc, nthreads)
 
@@ -154,4 +203,5 @@ def lib_path() -> str:
 
 
 __all__ = ["OracleLib", "attention", "attention_rows", "probabilities",
-           "attention_online", "default_threads", "lib_path"]
+           "attention_online", "attention_gqa", "attention_rows_gqa", "default_threads",
+           "lib_path"]

@@ -92,6 +92,7 @@ typedef struct {
     double *o, *lse;                 /* full-tensor outputs (fwd) */
     double *o_rows, *lse_rows;       /* per-request outputs (rows) */
     const int64_t *bh_idx, *row_idx; /* requests (rows); NULL for fwd */
+    int64_t H, Hkv;                  /* query heads, key/value heads */
     int64_t N, D;
     double scale;
     int causal;
@@ -119,8 +120,11 @@ static void* row_worker(void* arg)
             o_row = jb->o + it * D;
             lse_out = jb->lse ? jb->lse + it : NULL;
         }
-        const int64_t head = bh * N * D;
-        one_row(jb->q + head, jb->k + head, jb->v + head, N, D, jb->scale,
+        /* query head bh = b*H + h reads key/value head b*Hkv + h/(H/Hkv) */
+        const int64_t b = bh / jb->H, h = bh % jb->H;
+        const int64_t kvh = b * jb->Hkv + h / (jb->H / jb->Hkv);
+        const int64_t head = bh * N * D, kvhead = kvh * N * D;
+        one_row(jb->q + head, jb->k + kvhead, jb->v + kvhead, N, D, jb->scale,
                 jb->causal, i, s, o_row, lse_out);
     }
     free(s);
@@ -162,29 +166,43 @@ static int check_shape(int64_t B, int64_t H, int64_t N, int64_t D)
     return (B < 0 || H < 0 || N < 0 || D <= 0) ? -1 : 0;
 }
 
-int attn_oracle_fwd(const double* q, const double* k, const double* v,
-                    double* o, double* lse,
-                    int64_t B, int64_t H, int64_t N, int64_t D,
-                    double scale, int causal, int nthreads)
+static int check_heads(int64_t H, int64_t Hkv)
 {
-    if (check_shape(B, H, N, D)) return -1;
+    return (Hkv <= 0 && H > 0) || Hkv < 0 || (Hkv > 0 && H % Hkv != 0) ? -1 : 0;
+}
+
+int attn_oracle_fwd_gqa(const double* q, const double* k, const double* v,
+                        double* o, double* lse,
+                        int64_t B, int64_t H, int64_t Hkv, int64_t N, int64_t D,
+                        double scale, int causal, int nthreads)
+{
+    if (check_shape(B, H, N, D) || check_heads(H, Hkv)) return -1;
     int64_t nitems = B * H * N;
     if (nitems == 0) return 0;
     if (!q || !k || !v || !o) return -2;
     row_job p;
     memset(&p, 0, sizeof(p));
     p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+    p.H = H; p.Hkv = Hkv;
     p.N = N; p.D = D; p.scale = scale; p.causal = causal;
     return run_rows(p, nitems, nthreads);
 }
 
-int attn_oracle_rows(const double* q, const double* k, const double* v,
-                     int64_t B, int64_t H, int64_t N, int64_t D,
-                     double scale, int causal,
-                     const int64_t* bh_idx, const int64_t* row_idx, int64_t nrows,
-                     double* o_rows, double* lse_rows, int nthreads)
+int attn_oracle_fwd(const double* q, const double* k, const double* v,
+                    double* o, double* lse,
+                    int64_t B, int64_t H, int64_t N, int64_t D,
+                    double scale, int causal, int nthreads)
 {
-    if (check_shape(B, H, N, D) || nrows < 0) return -1;
+    return attn_oracle_fwd_gqa(q, k, v, o, lse, B, H, H, N, D, scale, causal, nthreads);
+}
+
+int attn_oracle_rows_gqa(const double* q, const double* k, const double* v,
+                         int64_t B, int64_t H, int64_t Hkv, int64_t N, int64_t D,
+                         double scale, int causal,
+                         const int64_t* bh_idx, const int64_t* row_idx, int64_t nrows,
+                         double* o_rows, double* lse_rows, int nthreads)
+{
+    if (check_shape(B, H, N, D) || check_heads(H, Hkv) || nrows < 0) return -1;
     if (nrows == 0) return 0;
     if (!q || !k || !v || !bh_idx || !row_idx || !o_rows) return -2;
     for (int64_t r = 0; r < nrows; ++r)
@@ -195,8 +213,19 @@ int attn_oracle_rows(const double* q, const double* k, const double* v,
     p.q = q; p.k = k; p.v = v;
     p.o_rows = o_rows; p.lse_rows = lse_rows;
     p.bh_idx = bh_idx; p.row_idx = row_idx;
+    p.H = H; p.Hkv = Hkv;
     p.N = N; p.D = D; p.scale = scale; p.causal = causal;
     return run_rows(p, nrows, nthreads);
+}
+
+int attn_oracle_rows(const double* q, const double* k, const double* v,
+                     int64_t B, int64_t H, int64_t N, int64_t D,
+                     double scale, int causal,
+                     const int64_t* bh_idx, const int64_t* row_idx, int64_t nrows,
+                     double* o_rows, double* lse_rows, int nthreads)
+{
+    return attn_oracle_rows_gqa(q, k, v, B, H, H, N, D, scale, causal, bh_idx, row_idx,
+                                nrows, o_rows, lse_rows, nthreads);
 }
 
 int attn_oracle_probs(const double* q, const double* k,

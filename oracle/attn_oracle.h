@@ -76,6 +76,26 @@ int attn_oracle_online_fwd(const double* q, const double* k, const double* v,
                            double scale, int causal, int64_t Br, int64_t Bc,
                            int nthreads);
 
+/* Grouped-query attention: q and o are [B,H,N,D], k and v are [B,Hkv,N,D]
+ * with H a multiple of Hkv; query head h reads key/value head
+ * h / (H/Hkv) of the same batch (consecutive query heads share a K/V head).
+ * Hkv == H is ordinary multi-head attention; Hkv == 1 is multi-query.
+ * Source: the GQA entry (Ainslie et al.) among the references of the
+ * chang-wenbin.github.io FA2 report; the head mapping itself is not on the
+ * pages and is the usual consecutive grouping. */
+int attn_oracle_fwd_gqa(const double* q, const double* k, const double* v,
+                        double* o, double* lse,
+                        int64_t B, int64_t H, int64_t Hkv, int64_t N, int64_t D,
+                        double scale, int causal, int nthreads);
+
+/* Selected rows of the grouped-query forward; bh_idx indexes query heads
+ * (b*H + h). */
+int attn_oracle_rows_gqa(const double* q, const double* k, const double* v,
+                         int64_t B, int64_t H, int64_t Hkv, int64_t N, int64_t D,
+                         double scale, int causal,
+                         const int64_t* bh_idx, const int64_t* row_idx, int64_t nrows,
+                         double* o_rows, double* lse_rows, int nthreads);
+
 /* Number of threads nthreads<=0 resolves to (CPUs in the affinity mask). */
 int attn_oracle_default_threads(void);
 

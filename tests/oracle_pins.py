@@ -240,7 +240,47 @@ def pin_golden_max_row(orc):
     assert g["max"] <= lse[0, 0, 0] <= g["max"] + math.log(N)
 
 
+def pin_gqa_equals_repeated_heads(orc):
+    """Grouped-query attention is multi-head attention on K/V heads repeated
+    H/Hkv times (consecutive query heads share one K/V head); Hkv = H is MHA."""
+    r = _rng(31)
+    B, H, N, D = 2, 6, 23, 8
+    q = r.standard_normal((B, H, N, D))
+    for Hkv in (1, 2, 3, 6):
+        k = r.standard_normal((B, Hkv, N, D))
+        v = r.standard_normal((B, Hkv, N, D))
+        krep = np.repeat(k, H // Hkv, axis=1)
+        vrep = np.repeat(v, H // Hkv, axis=1)
+        for causal in (False, True):
+            o, lse = orc.attention_gqa(q, k, v, 0.45, causal)
+            o2, lse2 = orc.attention(q, krep, vrep, 0.45, causal)
+            _close(o, o2, 0.0, "gqa O Hkv=%d" % Hkv)
+            _close(lse, lse2, 0.0, "gqa lse Hkv=%d" % Hkv)
+            bh = r.integers(0, B * H, 17)
+            ri = r.integers(0, N, 17)
+            orow, lrow = orc.attention_rows_gqa(q, k, v, 0.45, causal, bh, ri)
+            _close(orow, o.reshape(B * H, N, D)[bh, ri], 0.0, "gqa rows O")
+            _close(lrow, lse.reshape(B * H, N)[bh, ri], 0.0, "gqa rows lse")
+
+
+def pin_gqa_bruteforce(orc):
+    """Tiny multi-query case against the 40-digit decimal brute force run per
+    query head on its (shared) K/V head."""
+    r = _rng(32)
+    B, H, Hkv, N, D = 1, 4, 2, 5, 3
+    q = r.standard_normal((B, H, N, D))
+    k = r.standard_normal((B, Hkv, N, D))
+    v = r.standard_normal((B, Hkv, N, D))
+    for causal in (False, True):
+        o, lse = orc.attention_gqa(q, k, v, 0.7, causal)
+        for h in range(H):
+            kv = h // (H // Hkv)
+            ob, lb, _ = _decimal_attention(q[:, h:h + 1], k[:, kv:kv + 1], v[:, kv:kv + 1], 0.7, causal)
+            _close(o[:, h:h + 1], ob, 1e-13, "gqa brute O")
+            _close(lse[:, h:h + 1], lb, 1e-13, "gqa brute lse")
+
+
 ALL_PINS = [pin_row_sums, pin_ones_v, pin_zero_q, pin_basis_v, pin_shift_invariance,
             pin_single_key, pin_causal_first_rows, pin_permutation, pin_bruteforce,
             pin_rows_match_full, pin_online_matches_definition, pin_golden_dot,
-            pin_golden_max_row]
+            pin_golden_max_row, pin_gqa_equals_repeated_heads, pin_gqa_bruteforce]

@@ -45,6 +45,10 @@ MUTANTS = [
     ("online_drops_ragged_tile", "int64_t Tc = (kv_limit + Bc - 1) / Bc;", "int64_t Tc = kv_limit / Bc;"),
     ("online_mask_row_vs_block", "(diag && key > row)", "(diag && key > q_start)"),
     ("online_l_not_rescaled", "l[r] = corr * l[r] + lsum;", "l[r] = l[r] + lsum;"),
+    ("gqa_interleaved_heads", "const int64_t kvh = b * jb->Hkv + h / (jb->H / jb->Hkv);",
+     "const int64_t kvh = b * jb->Hkv + h % jb->Hkv;"),
+    ("gqa_no_batch_offset", "const int64_t kvh = b * jb->Hkv + h / (jb->H / jb->Hkv);",
+     "const int64_t kvh = h / (jb->H / jb->Hkv) + 0 * b;"),
 ]
 
 
