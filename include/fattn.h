@@ -96,6 +96,22 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, fl
               int dtype, fattn_stream_t stream);
 
 /*
+ * fattn_fwd_gqa -- grouped-query / multi-query attention forward.
+ *
+ * As fattn_fwd, except that k and v are [B, Hkv, N, D] with H a multiple of
+ * Hkv, and query head h of batch b attends to key/value head
+ * b*Hkv + h / (H/Hkv): consecutive groups of H/Hkv query heads share one
+ * K/V head (Hkv == H is fattn_fwd; Hkv == 1 is multi-query attention).
+ * Compatibility of the tiled method with GQA: the GQA reference (Ainslie et
+ * al.) cited by the chang-wenbin.github.io FA2 report; the head mapping is the
+ * usual consecutive grouping.  Hkv <= 0 or H % Hkv != 0 -> FATTN_ERR_INVALID_ARG.
+ * o and lse keep the query shapes [B,H,N,D] and [B,H,N].
+ */
+FATTN_API int fattn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int64_t B, int64_t H, int64_t Hkv, int64_t N, int64_t D, float scale,
+                  int causal, int dtype, fattn_stream_t stream);
+
+/*
  * fattn_fwd_host -- the same forward for callers holding the tensors in host
  * memory: enqueues on `stream` the host->device copies of q, k, v into the
  * caller's device buffers q_dev, k_dev, v_dev, the forward kernel writing

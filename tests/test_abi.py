@@ -32,8 +32,9 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     syms = declared_symbols()
-    for name in ("fattn_fwd", "fattn_fwd_host", "fattn_plan", "fattn_get_device_status",
-                 "fattn_selftest_wait_timeout", "fattn_status_string", "fattn_version"):
+    for name in ("fattn_fwd", "fattn_fwd_gqa", "fattn_fwd_host", "fattn_plan",
+                 "fattn_get_device_status", "fattn_selftest_wait_timeout",
+                 "fattn_status_string", "fattn_version"):
         assert name in syms
 
 
@@ -79,6 +80,24 @@ def test_argument_errors_before_any_cuda_call(lib):
     assert call_fwd(lib, N=(1 << 30) + 1) == UNSUPPORTED
     assert call_fwd(lib, B=1 << 16, H=1 << 16) == UNSUPPORTED
     assert call_fwd(lib, B=70000, H=1, dtype=0) == UNSUPPORTED
+
+
+def test_gqa_argument_errors(lib):
+    def gqa(H=8, Hkv=2, **kw):
+        args = dict(q=FAKE, k=FAKE + (1 << 16), v=FAKE + (2 << 16), o=FAKE + (3 << 16), lse=None,
+                    B=1, N=16, D=64, scale=0.125, causal=0, dtype=2)
+        args.update(kw)
+        return lib.fattn_fwd_gqa(args["q"], args["k"], args["v"], args["o"], args["lse"],
+                                 args["B"], H, Hkv, args["N"], args["D"], args["scale"],
+                                 args["causal"], args["dtype"], None)
+    assert gqa(Hkv=0) == INVALID
+    assert gqa(Hkv=-1) == INVALID
+    assert gqa(Hkv=3) == INVALID          # 8 % 3 != 0
+    assert gqa(Hkv=16) == INVALID         # more K/V heads than query heads
+    assert gqa(D=80) == UNSUPPORTED
+    assert gqa(H=0, Hkv=0) == OK          # empty problem
+    # O overlapping the (smaller) K tensor
+    assert gqa(o=FAKE + (1 << 16) + 64) == INVALID
 
 
 def test_empty_problem_is_ok_and_enqueues_nothing(lib):

@@ -62,6 +62,7 @@ def load():
     lib = ctypes.CDLL(_LIB_PATH)
     vp, i64, f32, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
     lib.fattn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, ci, ci, vp]
+    lib.fattn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, ci, ci, vp]
     lib.fattn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                    i64, i64, i64, i64, f32, ci, ci, vp]
     lib.fattn_plan.argtypes = [i64, i64, i64, i64, ci, ci, ci, ctypes.POINTER(i64)]
@@ -70,7 +71,7 @@ def load():
     lib.fattn_status_string.argtypes = [ci]
     lib.fattn_status_string.restype = ctypes.c_char_p
     lib.fattn_version.argtypes = []
-    for f in ("fattn_fwd", "fattn_fwd_host", "fattn_plan", "fattn_get_device_status",
+    for f in ("fattn_fwd", "fattn_fwd_gqa", "fattn_fwd_host", "fattn_plan", "fattn_get_device_status",
               "fattn_selftest_wait_timeout", "fattn_version"):
         getattr(lib, f).restype = ci
     _lib = lib
@@ -97,10 +98,16 @@ def _default_scale(D):
     return float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32).item())
 
 
-def _check_qkv(q, k, v):
-    if q.dim() != 4:
+def _check_qkv(q, k, v, allow_gqa=False):
+    if q.dim() != 4 or k.dim() != 4:
         raise ValueError("q, k, v must be [B, H, N, D]")
-    if k.shape != q.shape or v.shape != q.shape:
+    if v.shape != k.shape:
+        raise ValueError("k and v must have the same shape")
+    if allow_gqa:
+        B, H, N, D = q.shape
+        if k.shape[0] != B or k.shape[2] != N or k.shape[3] != D:
+            raise ValueError("k, v must be [B, Hkv, N, D] with q's B, N and D")
+    elif k.shape != q.shape:
         raise ValueError("q, k, v must have the same shape")
     if k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("q, k, v must have the same dtype")
@@ -114,17 +121,19 @@ def _check_qkv(q, k, v):
 def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, return_lse=True, stream=None):
     """Attention forward on CUDA tensors.
 
-    q, k, v: [B, H, N, D] contiguous CUDA tensors of one dtype (float32,
-    float16 or bfloat16), D in {64, 128}.  Returns (o, lse): o has q's dtype
+    q: [B, H, N, D]; k, v: [B, Hkv, N, D] with H a multiple of Hkv
+    (grouped-query attention when Hkv < H); contiguous CUDA tensors of one
+    dtype (float32, float16 or bfloat16), D in {64, 128}.  Returns (o, lse): o has q's dtype
     and shape; lse is float32 [B, H, N] (natural-log log-sum-exp of the
     scaled scores), or None when return_lse is False.  ``out`` / ``lse`` may
     be given to write into existing tensors.  Enqueued on ``stream`` (default:
     torch's current stream); no synchronisation.
     """
-    _check_qkv(q, k, v)
+    _check_qkv(q, k, v, allow_gqa=True)
     if not q.is_cuda:
         raise ValueError("fwd needs CUDA tensors; see fwd_host for host buffers")
     B, H, N, D = q.shape
+    Hkv = k.shape[1]
     if scale is None:
         scale = _default_scale(D)
     if out is None:
@@ -134,10 +143,15 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, return_lse=True, 
     lse_ptr = lse.data_ptr() if (return_lse and lse is not None) else None
     lib = load()
     with torch.cuda.device(q.device):
-        rc = lib.fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
-                           B, H, N, D, float(scale), int(bool(causal)), DTYPE_CODES[q.dtype],
-                           _stream_handle(stream))
-    _check(rc, "fattn_fwd")
+        if Hkv == H:
+            rc = lib.fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
+                               B, H, N, D, float(scale), int(bool(causal)), DTYPE_CODES[q.dtype],
+                               _stream_handle(stream))
+        else:
+            rc = lib.fattn_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                   lse_ptr, B, H, Hkv, N, D, float(scale), int(bool(causal)),
+                                   DTYPE_CODES[q.dtype], _stream_handle(stream))
+    _check(rc, "fattn_fwd" if Hkv == H else "fattn_fwd_gqa")
     return out, (lse if return_lse else None)
 
 

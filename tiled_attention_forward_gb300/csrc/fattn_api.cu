@@ -27,10 +27,12 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 // Validation shared by every compute entry point; returns FATTN_OK when the
 // call may proceed (which includes the empty problem, flagged by *empty).
 int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
-             int64_t B, int64_t H, int64_t N, int64_t D, float scale, int dtype, bool* empty) {
+             int64_t B, int64_t H, int64_t Hkv, int64_t N, int64_t D, float scale, int dtype,
+             bool* empty) {
     *empty = false;
     if (dtype != FATTN_F32 && dtype != FATTN_F16 && dtype != FATTN_BF16) return FATTN_ERR_INVALID_ARG;
     if (B < 0 || H < 0 || N < 0 || D < 0) return FATTN_ERR_INVALID_ARG;
+    if (H > 0 && (Hkv <= 0 || H % Hkv != 0)) return FATTN_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || scale < 0.f) return FATTN_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return FATTN_ERR_UNSUPPORTED;
     if (B == 0 || H == 0 || N == 0) {
@@ -48,12 +50,14 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FATTN_ERR_MISALIGNED;
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FATTN_ERR_MISALIGNED;
     const size_t bytes = static_cast<size_t>(BH * N * D) * elem_bytes(dtype);
-    if (overlaps(o, bytes, q, bytes) || overlaps(o, bytes, k, bytes) || overlaps(o, bytes, v, bytes))
+    const size_t kvbytes = static_cast<size_t>(B * Hkv * N * D) * elem_bytes(dtype);
+    if (overlaps(o, bytes, q, bytes) || overlaps(o, bytes, k, kvbytes) ||
+        overlaps(o, bytes, v, kvbytes))
         return FATTN_ERR_INVALID_ARG;
     if (lse) {
         const size_t lb = static_cast<size_t>(BH * N) * sizeof(float);
-        if (overlaps(lse, lb, o, bytes) || overlaps(lse, lb, q, bytes) || overlaps(lse, lb, k, bytes) ||
-            overlaps(lse, lb, v, bytes))
+        if (overlaps(lse, lb, o, bytes) || overlaps(lse, lb, q, bytes) ||
+            overlaps(lse, lb, k, kvbytes) || overlaps(lse, lb, v, kvbytes))
             return FATTN_ERR_INVALID_ARG;
     }
     return FATTN_OK;
@@ -98,20 +102,22 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 }  // namespace
 
 cudaError_t tc_encode_maps(TcArgs& a, const void* q, const void* k, const void* v, int64_t BH,
-                           int64_t N, int64_t D, bool bf16) {
+                           int64_t BHkv, int64_t N, int64_t D, bool bf16) {
     auto encode = get_encode_fn();
     if (!encode) return cudaErrorNotSupported;
     const CUtensorMapDataType dt =
         bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    // [B*H][N][D] row-major, 16-bit: innermost D, then rows, then heads.
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
-                                static_cast<cuuint64_t>(BH)};
+    // [heads][N][D] row-major, 16-bit: innermost D, then rows, then heads
+    // (B*H heads for Q, B*Hkv for K and V).
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 2), static_cast<cuuint64_t>(N * D * 2)};
     const cuuint32_t box[3] = {64, 128, 1};  // one 128-byte swizzle atom wide, 128 rows
     const cuuint32_t estr[3] = {1, 1, 1};
     const void* ptrs[3] = {q, k, v};
+    const int64_t heads[3] = {BH, BHkv, BHkv};
     CUtensorMap* maps[3] = {&a.tmap_q, &a.tmap_k, &a.tmap_v};
     for (int i = 0; i < 3; ++i) {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                                    static_cast<cuuint64_t>(heads[i])};
         CUresult r = encode(maps[i], dt, 3, const_cast<void*>(ptrs[i]), dims, strides, box, estr,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -198,8 +204,14 @@ int fattn_plan(int64_t B, int64_t H, int64_t N, int64_t D, int causal, int dtype
 
 int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
               int64_t N, int64_t D, float scale, int causal, int dtype, fattn_stream_t stream_h) {
+    return fattn_fwd_gqa(q, k, v, o, lse, B, H, H, N, D, scale, causal, dtype, stream_h);
+}
+
+int fattn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                  int64_t H, int64_t Hkv, int64_t N, int64_t D, float scale, int causal, int dtype,
+                  fattn_stream_t stream_h) {
     bool empty = false;
-    int st = validate(q, k, v, o, lse, B, H, N, D, scale, dtype, &empty);
+    int st = validate(q, k, v, o, lse, B, H, Hkv, N, D, scale, dtype, &empty);
     if (st != FATTN_OK || empty) return st;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
     const int64_t BH = B * H;
@@ -210,8 +222,8 @@ int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, 
         st = current_sm_count(&sms);
         if (st != FATTN_OK) return st;
         cudaError_t e = ffma_launch(static_cast<const float*>(q), static_cast<const float*>(k),
-                                    static_cast<const float*>(v), static_cast<float*>(o), lse, BH, N,
-                                    D, scale_log2, causal != 0, stream);
+                                    static_cast<const float*>(v), static_cast<float*>(o), lse, BH, H,
+                                    Hkv, N, D, scale_log2, causal != 0, stream);
         return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
     }
 
@@ -221,11 +233,13 @@ int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, 
     TcArgs a;
     std::memset(&a, 0, sizeof(a));
     const bool bf16 = dtype == FATTN_BF16;
-    if (tc_encode_maps(a, q, k, v, BH, N, D, bf16) != cudaSuccess) return FATTN_ERR_CUDA;
+    if (tc_encode_maps(a, q, k, v, BH, B * Hkv, N, D, bf16) != cudaSuccess) return FATTN_ERR_CUDA;
     a.o = o;
     a.lse = lse;
     a.N = static_cast<int>(N);
     a.BH = static_cast<int>(BH);
+    a.H = static_cast<int>(H);
+    a.Hkv = static_cast<int>(Hkv);
     a.num_qblk = static_cast<int>(ceil_div(N, int64_t(kTcBM) * kTcQTiles));
     a.num_tasks = a.num_qblk * a.BH;
     a.scale_log2 = scale_log2;
@@ -240,7 +254,7 @@ int fattn_fwd_host(const void* q_host, const void* k_host, const void* v_host, v
                    int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal, int dtype,
                    fattn_stream_t stream_h) {
     bool empty = false;
-    int st = validate(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, N, D, scale, dtype, &empty);
+    int st = validate(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, H, N, D, scale, dtype, &empty);
     if (st != FATTN_OK || empty) return st;
     if (!q_host || !k_host || !v_host || !o_host) return FATTN_ERR_INVALID_ARG;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);

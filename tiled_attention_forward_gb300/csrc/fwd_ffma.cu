@@ -80,7 +80,8 @@ template <int D, int BC, bool CAUSAL>
 __global__ void __launch_bounds__(kFfmaBr, 2)
     attn_fwd_ffma_kernel(const float* __restrict__ q, const float* __restrict__ k,
                          const float* __restrict__ v, float* __restrict__ o,
-                         float* __restrict__ lse, int N, int num_qblk, float scale_log2) {
+                         float* __restrict__ lse, int N, int num_qblk, int H, int Hkv,
+                         float scale_log2) {
     using L = FfmaLayout<D, BC>;
     extern __shared__ float4 smem4[];
     float* smem = reinterpret_cast<float*>(smem4);
@@ -93,9 +94,10 @@ __global__ void __launch_bounds__(kFfmaBr, 2)
     const int q_start = qblk * L::kBr;
     const int row = q_start + tid;
     const int64_t head = static_cast<int64_t>(blockIdx.y) * N * D;
+    const int64_t kvhead = static_cast<int64_t>(kv_head_of(blockIdx.y, H, Hkv)) * N * D;
     const float* qh = q + head;
-    const float* kh = k + head;
-    const float* vh = v + head;
+    const float* kh = k + kvhead;
+    const float* vh = v + kvhead;
 
     const int kv_limit = CAUSAL ? min(q_start + L::kBr, N) : N;
     const int Tc = (kv_limit + BC - 1) / BC;
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(kFfmaBr, 2)
 
 template <int D, int BC, bool CAUSAL>
 cudaError_t launch_ffma(const float* q, const float* k, const float* v, float* o, float* lse,
-                        int BH, int N, float scale_log2, cudaStream_t stream) {
+                        int BH, int H, int Hkv, int N, float scale_log2, cudaStream_t stream) {
     using L = FfmaLayout<D, BC>;
     auto* fn = attn_fwd_ffma_kernel<D, BC, CAUSAL>;
     static bool done[kMaxDevices] = {};
@@ -230,7 +232,7 @@ cudaError_t launch_ffma(const float* q, const float* k, const float* v, float* o
     }
     const int num_qblk = (N + L::kBr - 1) / L::kBr;
     dim3 grid(num_qblk, BH);
-    fn<<<grid, L::kBr, L::kBytes, stream>>>(q, k, v, o, lse, N, num_qblk, scale_log2);
+    fn<<<grid, L::kBr, L::kBytes, stream>>>(q, k, v, o, lse, N, num_qblk, H, Hkv, scale_log2);
     return cudaGetLastError();
 }
 
@@ -242,14 +244,15 @@ int ffma_smem_bytes(int D) {
 }
 
 cudaError_t ffma_launch(const float* q, const float* k, const float* v, float* o, float* lse,
-                        int64_t BH, int64_t N, int64_t D, float scale_log2, bool causal,
-                        cudaStream_t stream) {
+                        int64_t BH, int64_t H, int64_t Hkv, int64_t N, int64_t D,
+                        float scale_log2, bool causal, cudaStream_t stream) {
     const int bh = static_cast<int>(BH), n = static_cast<int>(N);
+    const int h = static_cast<int>(H), hk = static_cast<int>(Hkv);
     if (D == 64)
-        return causal ? launch_ffma<64, 32, true>(q, k, v, o, lse, bh, n, scale_log2, stream)
-                      : launch_ffma<64, 32, false>(q, k, v, o, lse, bh, n, scale_log2, stream);
-    return causal ? launch_ffma<128, 16, true>(q, k, v, o, lse, bh, n, scale_log2, stream)
-                  : launch_ffma<128, 16, false>(q, k, v, o, lse, bh, n, scale_log2, stream);
+        return causal ? launch_ffma<64, 32, true>(q, k, v, o, lse, bh, h, hk, n, scale_log2, stream)
+                      : launch_ffma<64, 32, false>(q, k, v, o, lse, bh, h, hk, n, scale_log2, stream);
+    return causal ? launch_ffma<128, 16, true>(q, k, v, o, lse, bh, h, hk, n, scale_log2, stream)
+                  : launch_ffma<128, 16, false>(q, k, v, o, lse, bh, h, hk, n, scale_log2, stream);
 }
 
 }  // namespace fattn

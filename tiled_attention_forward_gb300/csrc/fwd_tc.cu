@@ -190,7 +190,7 @@ __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
         __syncwarp();
         ++qcnt[i];
     };
-    auto load_kv = [&](const CUtensorMap* map, int j, int bh) {
+    auto load_kv = [&](const CUtensorMap* map, int j, int kvh) {
         const uint32_t slot = kv_it % L::kStages;
         const uint32_t round = kv_it / L::kStages;
         ok = warp_wait(&bars.kv_empty[slot], (round & 1u) ^ 1u, abort_flag, a.timeout_ns);
@@ -201,7 +201,7 @@ __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
 #pragma unroll
             for (int at = 0; at < L::kAtoms; ++at)
                 tma_load_3d_hint(dst + at * kTcBN * L::kAtomRowBytes, map, &bars.kv_full[slot],
-                                 at * 64, j * kTcBN, bh, keep);
+                                 at * 64, j * kTcBN, kvh, keep);
         }
         __syncwarp();
         ++kv_it;
@@ -209,17 +209,18 @@ __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
 
     for (int t = blockIdx.x; t < a.num_tasks && ok; t += gridDim.x) {
         const Task tk = decode_task<CAUSAL>(t, a);
+        const int kvh = kv_head_of(tk.bh, a.H, a.Hkv);
         load_q(0, tk);
         if (!ok) break;
-        load_kv(&a.tmap_k, 0, tk.bh);
+        load_kv(&a.tmap_k, 0, kvh);
         if (!ok) break;
         if (tk.nb[1] > 0) {
             load_q(1, tk);
             if (!ok) break;
         }
         for (int j = 0; j < tk.nbmax && ok; ++j) {
-            load_kv(&a.tmap_v, j, tk.bh);
-            if (ok && j + 1 < tk.nbmax) load_kv(&a.tmap_k, j + 1, tk.bh);
+            load_kv(&a.tmap_v, j, kvh);
+            if (ok && j + 1 < tk.nbmax) load_kv(&a.tmap_k, j + 1, kvh);
         }
     }
 

@@ -23,7 +23,9 @@ struct TcArgs {
     void* o;             // [B,H,N,D] output, input dtype
     float* lse;          // [B,H,N] or nullptr
     int N;
-    int BH;
+    int BH;              // B * H query heads (task space)
+    int H;               // query heads per batch
+    int Hkv;             // key/value heads per batch (H % Hkv == 0)
     int num_qblk;        // ceil(N / 256)
     int num_tasks;       // BH * num_qblk
     float scale_log2;    // scale * log2(e)
@@ -34,7 +36,7 @@ int tc_smem_bytes(int D);
 int tc_num_stages(int D);
 // Encodes the three tensor maps of `a` for these buffers (host).
 cudaError_t tc_encode_maps(TcArgs& a, const void* q, const void* k, const void* v, int64_t BH,
-                           int64_t N, int64_t D, bool bf16);
+                           int64_t BHkv, int64_t N, int64_t D, bool bf16);
 cudaError_t tc_launch(const TcArgs& a, int D, bool bf16, bool causal, int grid,
                       cudaStream_t stream);
 
@@ -43,8 +45,13 @@ constexpr int kFfmaBr = 128;      // Q rows per CTA = threads per CTA (one row p
 int ffma_bc(int D);               // keys per K/V tile
 int ffma_smem_bytes(int D);
 cudaError_t ffma_launch(const float* q, const float* k, const float* v, float* o, float* lse,
-                        int64_t BH, int64_t N, int64_t D, float scale_log2, bool causal,
-                        cudaStream_t stream);
+                        int64_t BH, int64_t H, int64_t Hkv, int64_t N, int64_t D,
+                        float scale_log2, bool causal, cudaStream_t stream);
+
+// Key/value head read by query head bh = b*H + h: b*Hkv + h / (H/Hkv).
+__host__ __device__ __forceinline__ int kv_head_of(int bh, int H, int Hkv) {
+    return (bh / H) * Hkv + (bh % H) / (H / Hkv);
+}
 
 // ---- device error word (fwd_tc.cu) -----------------------------------------
 cudaError_t read_and_clear_error_word(uint32_t* out);
