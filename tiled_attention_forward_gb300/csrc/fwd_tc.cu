@@ -319,33 +319,51 @@ __device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint3
         // iteration.
         for (int j = 0; j < tk.nbmax && ok; ++j) {
             const bool has_next = j + 1 < tk.nbmax;
+            // Any barrier test issued right after an MMA group waits for that
+            // group to be taken by the tensor pipe, so the tests are batched
+            // where that costs nothing else.  With a deep K/V ring (D = 64:
+            // eight stages) K_{j+1} has long landed when P_0 is ready, and V_j,
+            // K_{j+1}, P_0 are tested together before tile 0's MMAs.  With the
+            // five-stage ring of D = 128 a K tile is often still in flight
+            // then, so P.V_0 is issued first and K_{j+1} waited for after it.
+            constexpr bool kEarlyK = L::kStages >= 8;
             wait_slot(vslot);  // V_j
             if (!ok) break;
+            if (kEarlyK && has_next) {
+                wait_slot(kslot);  // K_{j+1}
+                if (!ok) break;
+            }
             for (int i = 0; i < 2 && ok; ++i) {
                 if (j < tk.nb[i]) {
                     ok = warp_wait(&bars.p_full[i], pcnt[i] & 1u, abort_flag, a.timeout_ns);
                     ++pcnt[i];
                     if (!ok) break;
                     tc_fence_after();
-                    if (elect_one_sync()) {
-                        issue_pv(i, vslot, j > 0);
-                        if (j == tk.nb[i] - 1) mma_commit(&bars.o_full[i]);
+                    if (!kEarlyK) {
+                        if (elect_one_sync()) {
+                            issue_pv(i, vslot, j > 0);
+                            if (j == tk.nb[i] - 1) mma_commit(&bars.o_full[i]);
+                        }
+                        __syncwarp();
                     }
-                    __syncwarp();
                 }
-                if (i == 0 && has_next) {
+                if (!kEarlyK && i == 0 && has_next) {
                     wait_slot(kslot);  // K_{j+1}
                     if (!ok) break;
                 }
-                if (j + 1 < tk.nb[i]) {
-                    if (elect_one_sync()) {
+                if (elect_one_sync()) {
+                    if (kEarlyK && j < tk.nb[i]) {
+                        issue_pv(i, vslot, j > 0);
+                        if (j == tk.nb[i] - 1) mma_commit(&bars.o_full[i]);
+                    }
+                    if (j + 1 < tk.nb[i]) {
                         issue_qk(i, kslot);
                         mma_commit(&bars.s_full[i]);
                         if (j + 1 == tk.nb[i] - 1) mma_commit(&bars.q_empty[i]);
                     }
-                    __syncwarp();
-                    if (j + 1 == tk.nb[i] - 1) ++qcnt[i];
                 }
+                __syncwarp();
+                if (j + 1 < tk.nb[i] && j + 1 == tk.nb[i] - 1) ++qcnt[i];
             }
             if (!ok) break;
             // V_j and K_{j+1} are released once every MMA issued so far is done.
