@@ -49,9 +49,9 @@ METRIC = "attn fwd TFLOP/s (B=4,H=16,N=4096,D=128 bf16) and % of GB300 BF16 peak
 # while the sources still hash the same; null once the kernel has changed.
 KERNEL_SOURCES = ["fwd_tc.cu", "fwd_ffma.cu", "sm103_ptx.cuh", "internal.h", "fattn_api.cu"]
 NCU_TRAFFIC = {
-    "bf16_B4_H16_N4096_D128": (201609472 + 37907712, "2a19fa906990269c"),
-    "fp16_B1_H16_N16000_D64_causal": (125040128 + 15502080, "2a19fa906990269c"),
-    "fp32_B4_H8_N8192_D64_causal": (202531584 + 52426752, "2a19fa906990269c"),
+    "bf16_B4_H16_N4096_D128": (201420288 + 37305088, "05970775ad5b4aaf"),
+    "bf16_B2_H32_N8192_D128_causal_qstd4": (2468442000 + 128103936, "05970775ad5b4aaf"),
+    "fp16_B1_H16_N16000_D64_causal": (127311616 + 14989568, "05970775ad5b4aaf"),
 }
 
 
