@@ -1,6 +1,7 @@
 """Benchmark of the attention forward on GB300 (one JSON line on stdout).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference|unfused]
 
 A step is one attention forward (the whole hot path: one kernel launch) over
 the named workload's synthetic seeded inputs, already resident in HBM.
@@ -21,6 +22,11 @@ pinned memory, the kernel and the device->host copy of O and LSE.
 `cpu_baseline` is the fp64 CPU oracle as it stands, timed on this host's cores
 on a bounded sample of the same workload (a set of random query rows).
 `--impl reference` times that oracle alone (the reference arm of this method).
+
+`--impl unfused` times the library's materialising comparator
+(fattn_fwd_unfused: S and P written to HBM, three kernels per step) on the
+same workload, inputs and timing rules, for the HBM-traffic comparison; its
+roofline is the HBM bound of the whole three-kernel step.
 """
 import argparse
 import json
@@ -111,6 +117,28 @@ def w_bytes(w):
     """Compulsory HBM bytes of one forward: read Q, K, V once, write O and LSE once."""
     e = {"fp32": 4, "fp16": 2, "bf16": 2}[w.dtype]
     return 4 * w.B * w.H * w.N * w.D * e + 4 * w.B * w.H * w.N
+
+
+def unfused_bytes(w):
+    """Algorithmic HBM bytes of one materialising forward: Q, K, V read and O,
+    LSE written once, plus every computed S element written (fp32) and read
+    once and every P element the P V product reads written and read once
+    (16-bit).  Computed elements: 128 x 128 score tiles on or below the
+    diagonal under causal masking, all N x N otherwise."""
+    e = {"fp16": 2, "bf16": 2}[w.dtype]
+    nt = -(-w.N // 128)
+    npitch = -(-w.N // 8) * 8
+    if w.causal:
+        s_elems = 0
+        p_elems = 0
+        for qt in range(nt):
+            rows = min(128, w.N - qt * 128)
+            s_elems += rows * min(npitch, (qt + 1) * 128)
+            p_elems += rows * min(npitch, (qt + 1) * 128)
+    else:
+        s_elems = p_elems = w.N * npitch
+    bh = w.B * w.H
+    return w_bytes(w) + bh * (2 * 4 * s_elems + 2 * e * p_elems)
 
 
 def config_of(w, n_gpus):
@@ -231,8 +259,18 @@ def run_ours(args, w, ws, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    unfused = args.impl == "unfused"
+    if unfused:
+        if w.dtype == "fp32":
+            raise SystemExit("--impl unfused covers bf16 / fp16 workloads only")
+        wsp = torch.empty(fattn.unfused_workspace_bytes(w.B, w.H, w.N), dtype=torch.uint8, device=dev)
+
     def step():
-        fattn.fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream)
+        if unfused:
+            fattn.fwd_unfused(qd, kd, vd, causal=w.causal, scale=w.scale, out=o, lse=lse,
+                              workspace=wsp, stream=stream)
+        else:
+            fattn.fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream)
 
     def barrier():
         if ws > 1:
@@ -267,11 +305,12 @@ def run_ours(args, w, ws, rank, local):
         raise RuntimeError("device status %s during the timed region" % fattn.status_string(status))
     per = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
     ms_total = float(sum(per))
-    launches = args.steps  # fattn_fwd launches exactly one kernel per call
+    # fattn_fwd launches exactly one kernel per call, fattn_fwd_unfused three
+    launches = args.steps * (3 if unfused else 1)
 
     # end to end through the host-buffer entry point
     e2e_ms, h2d, d2h = float("nan"), 0, 0
-    if not args.no_e2e:
+    if not args.no_e2e and not unfused:
         e2e_ms, h2d, d2h = run_e2e(fattn, w, q, k, v, qd, kd, vd, o, lse, stream, dev, args.steps, barrier)
     ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], device=dev)
     clocks = sampler.summary(t0, t1)
@@ -286,7 +325,15 @@ def run_ours(args, w, ws, rank, local):
     achieved = flops / (ms_per_step * 1e-3) / 1e12  # one launch = one step on this GPU
     peaks, peak_src = load_peaks()
     peak_key = "bf16_tflops"
-    if w.dtype == "fp32":
+    if unfused:
+        gbs = unfused_bytes(w) / (ms_per_step * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                "traffic": None, "scope": "the whole three-kernel step (S, softmax, P V)",
+                "peak_source": "hbm_gbs (STREAM-style copy) of %s" % peak_src,
+                "algorithmic_bytes": unfused_bytes(w),
+                "tensor_tflops": achieved}
+    elif w.dtype == "fp32":
         sm_mhz = peaks.get("sm_max_mhz", 2070.0)
         peak = torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT,
@@ -299,8 +346,12 @@ def run_ours(args, w, ws, rank, local):
                 "peak_source": "%s dense bf16 (cuBLAS burst) of %s; fp16 taken at the same rate"
                                % (peak_key, peak_src),
                 "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak))}
-    roof["traffic_note"] = ("DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum); "
+    roof["traffic_note"] = "see profiles/ for ncu DRAM bytes" if unfused else ("DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum); "
                             "algorithmic compulsory bytes (Q+K+V read, O+LSE write): %d" % w_bytes(w))
+    if unfused:
+        line_extra = {"impl": "unfused"}
+    else:
+        line_extra = {}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_median": statistics.median(per),
@@ -310,10 +361,11 @@ def run_ours(args, w, ws, rank, local):
         "e2e": ({"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                  "ms_per_step": e2e_ms, "api": "fattn_fwd_host (pinned host buffers)"}
-                if not args.no_e2e else None),
+                if not (args.no_e2e or unfused) else None),
         "gpu_launches": launches, "clocks": clocks,
     }
-    if not args.no_cpu_baseline:
+    line.update(line_extra)
+    if not args.no_cpu_baseline and not unfused:
         q64, k64, v64 = (t.to(torch.float64).numpy() for t in (q, k, v))
         fl, secs, nrows, threads = oracle_rows_rate(w, q64, k64, v64, args.cpu_seconds, 1)
         line["cpu_baseline"] = {"value": fl / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -382,13 +434,13 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference", "unfused"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall time of the CPU oracle sample (cpu_baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     args = ap.parse_args()
-    if args.warmup < 3 and args.impl == "ours":
+    if args.warmup < 3 and args.impl != "reference":
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_env()
     w = BY_NAME[args.workload]

@@ -130,6 +130,44 @@ FATTN_API int fattn_fwd_host(const void* q_host, const void* k_host, const void*
                    int dtype, fattn_stream_t stream);
 
 /*
+ * fattn_unfused_workspace_bytes -- bytes of device workspace fattn_fwd_unfused
+ * needs for B*H heads of length N: S fp32 [B*H][N][Np] followed by P 16-bit
+ * [B*H][N][Np], Np = N rounded up to a multiple of 8, i.e. 6 * B*H*N*Np.
+ * Returns 0 for an empty or invalid (negative, overflowing) size.
+ */
+FATTN_API int64_t fattn_unfused_workspace_bytes(int64_t B, int64_t H, int64_t N);
+
+/*
+ * fattn_fwd_unfused -- the same O and LSE computed the materialising way, as
+ * the comparator for the fused kernel's HBM traffic: three kernels, (1) S =
+ * scale Q K^T written to the workspace in fp32 (tcgen05, 128x128 tiles; under
+ * causal masking tiles wholly above the diagonal are skipped), (2) a row
+ * softmax reading S and writing P in the input dtype and the LSE, (3) O = P V
+ * (tcgen05) reading P back.  The three steps are the ScaledDotProduct ->
+ * Softmax -> PVMultiply pipeline of the cishoon.github.io "flashattention"
+ * page (§2), whose HBM traffic the chang-wenbin.github.io FA2 report (§3)
+ * contrasts with the fused form.
+ *
+ *   q,k,v,o,lse,B,H,N,D,scale,causal : as fattn_fwd.
+ *   dtype     : FATTN_BF16 or FATTN_F16 (FATTN_F32 -> FATTN_ERR_UNSUPPORTED).
+ *   workspace : caller-owned device buffer of at least
+ *               fattn_unfused_workspace_bytes(B, H, N) bytes, 16-byte aligned,
+ *               overlapping none of q, k, v, o, lse; its contents on entry are
+ *               ignored and on return are the S and P matrices (layout above;
+ *               S entries of skipped tiles and P entries past the last tile a
+ *               row's Q tile reads are left untouched).
+ *   workspace_bytes : its size; smaller than needed -> FATTN_ERR_INVALID_ARG.
+ *
+ * B*H and ceil(N/128) must each be <= 65535 (grid limits), else
+ * FATTN_ERR_UNSUPPORTED.  Three kernel launches per call on `stream`; no
+ * allocation.  Errors as fattn_fwd.
+ */
+FATTN_API int fattn_fwd_unfused(const void* q, const void* k, const void* v, void* o, float* lse,
+                      void* workspace, int64_t workspace_bytes, int64_t B, int64_t H,
+                      int64_t N, int64_t D, float scale, int causal, int dtype,
+                      fattn_stream_t stream);
+
+/*
  * fattn_plan -- host-only description of the launch fattn_fwd would make for
  * these arguments (no CUDA call when num_sms > 0).  Fills `out` with:
  *   out[0] path       : 0 = none (empty problem), 1 = FFMA fp32, 2 = tcgen05 bf16/fp16

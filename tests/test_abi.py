@@ -34,6 +34,7 @@ def test_header_declares_the_boundary():
     syms = declared_symbols()
     for name in ("fattn_fwd", "fattn_fwd_gqa", "fattn_fwd_host", "fattn_plan",
                  "fattn_get_device_status", "fattn_selftest_wait_timeout",
+                 "fattn_fwd_unfused", "fattn_unfused_workspace_bytes",
                  "fattn_status_string", "fattn_version"):
         assert name in syms
 
@@ -100,6 +101,36 @@ def test_gqa_argument_errors(lib):
     assert gqa(o=FAKE + (1 << 16) + 64) == INVALID
 
 
+def test_unfused_workspace_bytes(lib):
+    pitch = lambda n: (n + 7) // 8 * 8
+    for (B, H, N) in ((1, 1, 1), (2, 3, 17), (4, 16, 4096), (1, 16, 16000), (2, 32, 8192)):
+        assert lib.fattn_unfused_workspace_bytes(B, H, N) == 6 * B * H * N * pitch(N)
+    for (B, H, N) in ((0, 1, 1), (1, 0, 1), (1, 1, 0), (-1, 1, 1), (1 << 31, 1, 1 << 20)):
+        assert lib.fattn_unfused_workspace_bytes(B, H, N) == 0
+
+
+def test_unfused_argument_errors(lib):
+    WS = FAKE + (8 << 20)
+
+    def unf(ws=WS, wsb=None, B=1, H=2, N=16, D=64, dtype=2, **kw):
+        args = dict(q=FAKE, k=FAKE + (1 << 16), v=FAKE + (2 << 16), o=FAKE + (3 << 16), lse=None)
+        args.update(kw)
+        if wsb is None:
+            wsb = lib.fattn_unfused_workspace_bytes(B, H, N)
+        return lib.fattn_fwd_unfused(args["q"], args["k"], args["v"], args["o"], args["lse"],
+                                     ws, wsb, B, H, N, D, 0.125, 0, dtype, None)
+    assert unf(dtype=0) == UNSUPPORTED                  # fp32 has no comparator
+    assert unf(D=96) == UNSUPPORTED
+    assert unf(ws=None) == INVALID
+    assert unf(wsb=100) == INVALID                      # smaller than needed
+    assert unf(ws=WS + 4) == MISALIGNED
+    assert unf(ws=FAKE + (2 << 16)) == INVALID          # overlaps v
+    far = dict(q=1 << 40, k=2 << 40, v=3 << 40, o=4 << 40, ws=5 << 40, wsb=1 << 40)
+    assert unf(B=70000, H=1, **far) == UNSUPPORTED      # grid limit on B*H
+    assert unf(B=0) == OK                               # empty problem
+    assert unf(q=None) == INVALID
+
+
 def test_empty_problem_is_ok_and_enqueues_nothing(lib):
     for (B, H, N) in ((0, 4, 16), (2, 0, 16), (2, 4, 0)):
         assert call_fwd(lib, q=None, k=None, v=None, o=None, B=B, H=H, N=N) == OK
@@ -109,6 +140,9 @@ def test_empty_problem_is_ok_and_enqueues_nothing(lib):
 def test_valid_call_without_a_device_reports_no_device(lib):
     assert call_fwd(lib) == NO_DEVICE
     assert call_fwd(lib, dtype=0) == NO_DEVICE
+    ws = FAKE + (8 << 20)
+    assert lib.fattn_fwd_unfused(FAKE, FAKE + (1 << 16), FAKE + (2 << 16), FAKE + (3 << 16), None,
+                                 ws, 1 << 20, 1, 1, 16, 64, 0.125, 1, 2, None) == NO_DEVICE
     assert lib.fattn_selftest_wait_timeout(1000, None) == NO_DEVICE
     assert lib.fattn_selftest_wait_timeout(0, None) == INVALID
 

@@ -56,3 +56,20 @@ def test_workloads_are_the_five_headline_configs():
 def test_small_workload_inputs_shape():
     q, k, v = workload_inputs(WORKLOADS[0])
     assert q.shape == (1, 1, 256, 64) and q.dtype == torch.float32
+
+
+def test_unfused_algorithmic_bytes():
+    """bench.py's byte count for the materialising comparator: non-causal, S
+    (fp32) and P (16-bit) each written and read once over N x Np per head;
+    causal, only the rows' 128-key tiles on or below the diagonal."""
+    import bench
+    from tiled_attention_forward_gb300.inputs import BY_NAME
+    w = BY_NAME["bf16_B4_H16_N4096_D128"]
+    assert bench.unfused_bytes(w) == bench.w_bytes(w) + 64 * 4096 * 4096 * (8 + 4)
+    w = BY_NAME["fp16_B1_H16_N16000_D64_causal"]
+    nt = 125  # 16000 = 125 tiles of 128
+    elems = sum(128 * (qt + 1) * 128 for qt in range(nt))
+    assert bench.unfused_bytes(w) == bench.w_bytes(w) + 16 * elems * (8 + 4)
+    # a causal S/P triangle costs a bit over half of the square
+    full = 16000 * 16000
+    assert 0.5 < elems / full < 0.51

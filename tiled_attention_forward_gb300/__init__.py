@@ -18,7 +18,7 @@ import os
 
 import torch
 
-__all__ = ["fwd", "fwd_host", "plan", "get_device_status", "selftest_wait_timeout",
+__all__ = ["fwd", "fwd_host", "fwd_unfused", "unfused_workspace_bytes", "plan", "get_device_status", "selftest_wait_timeout",
            "status_string", "library_path", "load", "FattnError", "FattnLibraryMissing",
            "DTYPE_CODES", "STATUS"]
 
@@ -65,13 +65,17 @@ def load():
     lib.fattn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, ci, ci, vp]
     lib.fattn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                    i64, i64, i64, i64, f32, ci, ci, vp]
+    lib.fattn_fwd_unfused.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, ci,
+                                      ci, vp]
+    lib.fattn_unfused_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.fattn_unfused_workspace_bytes.restype = i64
     lib.fattn_plan.argtypes = [i64, i64, i64, i64, ci, ci, ci, ctypes.POINTER(i64)]
     lib.fattn_get_device_status.argtypes = [vp]
     lib.fattn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.fattn_status_string.argtypes = [ci]
     lib.fattn_status_string.restype = ctypes.c_char_p
     lib.fattn_version.argtypes = []
-    for f in ("fattn_fwd", "fattn_fwd_gqa", "fattn_fwd_host", "fattn_plan", "fattn_get_device_status",
+    for f in ("fattn_fwd", "fattn_fwd_gqa", "fattn_fwd_host", "fattn_fwd_unfused", "fattn_plan", "fattn_get_device_status",
               "fattn_selftest_wait_timeout", "fattn_version"):
         getattr(lib, f).restype = ci
     _lib = lib
@@ -175,6 +179,43 @@ def fwd_host(q_host, k_host, v_host, q_dev, k_dev, v_dev, o_dev, o_host, lse_dev
                                 B, H, N, D, float(scale), int(bool(causal)),
                                 DTYPE_CODES[q_host.dtype], _stream_handle(stream))
     _check(rc, "fattn_fwd_host")
+
+
+def unfused_workspace_bytes(B, H, N):
+    """Bytes of workspace fwd_unfused needs (S fp32 then P 16-bit, rows padded to 8)."""
+    return int(load().fattn_unfused_workspace_bytes(int(B), int(H), int(N)))
+
+
+def fwd_unfused(q, k, v, causal=False, scale=None, out=None, lse=None, workspace=None,
+                return_lse=True, stream=None):
+    """The materialising comparator: S = scale Q K^T and P = softmax(S) are
+    written to ``workspace`` (a CUDA uint8 tensor of at least
+    ``unfused_workspace_bytes(B, H, N)`` bytes; allocated here when None) and
+    O = P V is computed from P.  bfloat16 / float16 only, q, k, v of one shape.
+    Returns (o, lse) like ``fwd``."""
+    _check_qkv(q, k, v)
+    if not q.is_cuda:
+        raise ValueError("fwd_unfused needs CUDA tensors")
+    B, H, N, D = q.shape
+    if scale is None:
+        scale = _default_scale(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    need = unfused_workspace_bytes(B, H, N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    lse_ptr = lse.data_ptr() if (return_lse and lse is not None) else None
+    lib = load()
+    with torch.cuda.device(q.device):
+        rc = lib.fattn_fwd_unfused(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                   lse_ptr, workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(), B, H, N, D,
+                                   float(scale), int(bool(causal)), DTYPE_CODES[q.dtype],
+                                   _stream_handle(stream))
+    _check(rc, "fattn_fwd_unfused")
+    return out, (lse if return_lse else None)
 
 
 def plan(B, H, N, D, causal=False, dtype=torch.bfloat16, num_sms=0):

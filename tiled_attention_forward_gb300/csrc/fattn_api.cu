@@ -126,6 +126,24 @@ cudaError_t tc_encode_maps(TcArgs& a, const void* q, const void* k, const void* 
     return cudaSuccess;
 }
 
+cudaError_t unfused_encode_p_map(UnfusedArgs& a, int64_t BH, int64_t N, bool bf16) {
+    auto encode = get_encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    const int64_t np = unfused_row_pitch(N);
+    const CUtensorMapDataType dt =
+        bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    // P: [B*H][N][Np] 16-bit; keys innermost, 64 keys (128 bytes) per box row
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(np), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(np * 2), static_cast<cuuint64_t>(N * np * 2)};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(&a.tmap_p, dt, 3, a.p, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace fattn
 
 using namespace fattn;
@@ -274,11 +292,72 @@ int fattn_fwd_host(const void* q_host, const void* k_host, const void* v_host, v
     return FATTN_OK;
 }
 
+int64_t fattn_unfused_workspace_bytes(int64_t B, int64_t H, int64_t N) {
+    if (B <= 0 || H <= 0 || N <= 0) return 0;
+    if (B > (int64_t(1) << 30) || H > (int64_t(1) << 30) || N > (int64_t(1) << 30)) return 0;
+    const int64_t BH = B * H;
+    const int64_t np = unfused_row_pitch(N);
+    // 6 * BH * N * np must stay below 2^62
+    if (BH > (int64_t(1) << 30) || static_cast<double>(BH) * N * np * 6.0 > 4.0e18) return 0;
+    return static_cast<int64_t>(unfused_workspace_bytes(BH, N));
+}
+
+int fattn_fwd_unfused(const void* q, const void* k, const void* v, void* o, float* lse,
+                      void* workspace, int64_t workspace_bytes, int64_t B, int64_t H, int64_t N,
+                      int64_t D, float scale, int causal, int dtype, fattn_stream_t stream_h) {
+    bool empty = false;
+    int st = validate(q, k, v, o, lse, B, H, H, N, D, scale, dtype, &empty);
+    if (st != FATTN_OK || empty) return st;
+    if (dtype == FATTN_F32) return FATTN_ERR_UNSUPPORTED;
+    const int64_t BH = B * H;
+    if (BH > 65535 || ceil_div(N, 128) > 65535) return FATTN_ERR_UNSUPPORTED;
+    const int64_t need = fattn_unfused_workspace_bytes(B, H, N);
+    if (need <= 0) return FATTN_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < need) return FATTN_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return FATTN_ERR_MISALIGNED;
+    const size_t bytes = static_cast<size_t>(BH * N * D) * 2u;
+    const size_t ws = static_cast<size_t>(need);
+    if (overlaps(workspace, ws, q, bytes) || overlaps(workspace, ws, k, bytes) ||
+        overlaps(workspace, ws, v, bytes) || overlaps(workspace, ws, o, bytes) ||
+        (lse && overlaps(workspace, ws, lse, static_cast<size_t>(BH * N) * sizeof(float))))
+        return FATTN_ERR_INVALID_ARG;
+    int sms = 0;
+    st = current_sm_count(&sms);
+    if (st != FATTN_OK) return st;
+    UnfusedArgs a;
+    std::memset(&a, 0, sizeof(a));
+    const bool bf16 = dtype == FATTN_BF16;
+    TcArgs t;
+    std::memset(&t, 0, sizeof(t));
+    if (tc_encode_maps(t, q, k, v, BH, BH, N, D, bf16) != cudaSuccess) return FATTN_ERR_CUDA;
+    a.tmap_q = t.tmap_q;
+    a.tmap_k = t.tmap_k;
+    a.tmap_v = t.tmap_v;
+    a.s = static_cast<float*>(workspace);
+    a.p = static_cast<uint8_t*>(workspace) + static_cast<size_t>(BH * N * unfused_row_pitch(N)) * 4u;
+    if (unfused_encode_p_map(a, BH, N, bf16) != cudaSuccess) return FATTN_ERR_CUDA;
+    a.o = o;
+    a.lse = lse;
+    a.N = static_cast<int>(N);
+    a.Np = static_cast<int>(unfused_row_pitch(N));
+    a.BH = static_cast<int>(BH);
+    a.H = static_cast<int>(H);
+    a.Hkv = static_cast<int>(H);
+    a.scale = scale;
+    a.timeout_ns = kDefaultTimeoutNs;
+    cudaError_t e = unfused_launch(a, static_cast<int>(D), bf16, causal != 0,
+                                   reinterpret_cast<cudaStream_t>(stream_h));
+    return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
 int fattn_get_device_status(fattn_stream_t stream_h) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FATTN_ERR_CUDA;
-    uint32_t word = 0;
-    if (read_and_clear_error_word(&word) != cudaSuccess) return FATTN_ERR_CUDA;
+    uint32_t word = 0, word_unfused = 0;
+    if (read_and_clear_error_word(&word) != cudaSuccess ||
+        unfused_read_and_clear_error_word(&word_unfused) != cudaSuccess)
+        return FATTN_ERR_CUDA;
+    word |= word_unfused;
     if (word & (1u << FATTN_ERR_INTERNAL)) return FATTN_ERR_INTERNAL;
     if (word & (1u << FATTN_ERR_TIMEOUT)) return FATTN_ERR_TIMEOUT;
     return FATTN_OK;

@@ -48,6 +48,31 @@ cudaError_t ffma_launch(const float* q, const float* k, const float* v, float* o
                         int64_t BH, int64_t H, int64_t Hkv, int64_t N, int64_t D,
                         float scale_log2, bool causal, cudaStream_t stream);
 
+// ---- unfused comparator (bf16 / fp16), fwd_unfused.cu ----------------------
+struct UnfusedArgs {
+    CUtensorMap tmap_q;  // as TcArgs: 3-D {D, N, heads}, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tmap_k;
+    CUtensorMap tmap_v;
+    CUtensorMap tmap_p;  // 3-D {Np, N, B*H} over the P part of the workspace, same box
+    float* s;            // workspace: S fp32 [B*H][N][Np]
+    void* p;             // workspace: P 16-bit [B*H][N][Np]
+    void* o;             // [B,H,N,D] output, input dtype
+    float* lse;          // [B,H,N] or nullptr
+    int N;
+    int Np;              // row pitch of S and P in elements (N rounded up to 8)
+    int BH;
+    int H;
+    int Hkv;
+    float scale;         // natural-log units (S = scale Q K^T)
+    uint64_t timeout_ns;
+};
+
+int64_t unfused_row_pitch(int64_t N);
+size_t unfused_workspace_bytes(int64_t BH, int64_t N);
+cudaError_t unfused_encode_p_map(UnfusedArgs& a, int64_t BH, int64_t N, bool bf16);
+cudaError_t unfused_launch(const UnfusedArgs& a, int D, bool bf16, bool causal, cudaStream_t s);
+cudaError_t unfused_read_and_clear_error_word(uint32_t* out);
+
 // Key/value head read by query head bh = b*H + h: b*Hkv + h / (H/Hkv).
 __host__ __device__ __forceinline__ int kv_head_of(int bh, int H, int Hkv) {
     return (bh / H) * Hkv + (bh % H) / (H / Hkv);
