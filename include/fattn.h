@@ -168,6 +168,32 @@ FATTN_API int fattn_fwd_unfused(const void* q, const void* k, const void* v, voi
                       fattn_stream_t stream);
 
 /*
+ * fattn_fwd_unfused_static -- fattn_fwd_unfused with the workspace taken from
+ * a fixed array of FATTN_UNFUSED_STATIC_BYTES in the library's own static
+ * device memory (one per device) instead of from the caller, so that neither
+ * the caller nor the library allocates anything for the call.  The pages have
+ * no counterpart: it is an interface convenience around the same three
+ * kernels, which give bit-identical O, LSE, S and P.
+ *
+ *   Arguments and errors as fattn_fwd_unfused without workspace /
+ *   workspace_bytes.  A problem whose fattn_unfused_workspace_bytes(B, H, N)
+ *   exceeds FATTN_UNFUSED_STATIC_BYTES -> FATTN_ERR_UNSUPPORTED, before any
+ *   CUDA call.  Nothing in the array needs to start at zero: every element a
+ *   call reads is written earlier in the same call.
+ *
+ * Races: the array is shared by every call on a device.  Calls on one device
+ * must not overlap in time: enqueue them on one stream, or order them (events,
+ * synchronisation).  Overlapping calls race on S and P and leave O undefined.
+ * The first call on each device looks up the array's address
+ * (cudaGetSymbolAddress, under a host mutex) and sets the kernels' shared
+ * memory attributes; make that first call before any stream capture starts.
+ */
+#define FATTN_UNFUSED_STATIC_BYTES (64ll << 20)
+FATTN_API int fattn_fwd_unfused_static(const void* q, const void* k, const void* v, void* o,
+                             float* lse, int64_t B, int64_t H, int64_t N, int64_t D,
+                             float scale, int causal, int dtype, fattn_stream_t stream);
+
+/*
  * fattn_plan -- host-only description of the launch fattn_fwd would make for
  * these arguments (no CUDA call when num_sms > 0).  Fills `out` with:
  *   out[0] path       : 0 = none (empty problem), 1 = FFMA fp32, 2 = tcgen05 bf16/fp16

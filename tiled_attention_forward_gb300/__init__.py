@@ -18,7 +18,8 @@ import os
 
 import torch
 
-__all__ = ["fwd", "fwd_host", "fwd_unfused", "unfused_workspace_bytes", "plan", "get_device_status", "selftest_wait_timeout",
+__all__ = ["fwd", "fwd_host", "fwd_unfused", "fwd_unfused_static", "unfused_workspace_bytes",
+           "UNFUSED_STATIC_BYTES", "plan", "get_device_status", "selftest_wait_timeout",
            "status_string", "library_path", "load", "FattnError", "FattnLibraryMissing",
            "DTYPE_CODES", "STATUS"]
 
@@ -29,6 +30,7 @@ DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 STATUS = {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPORTED",
           3: "FATTN_ERR_MISALIGNED", 4: "FATTN_ERR_CUDA", 5: "FATTN_ERR_TIMEOUT",
           6: "FATTN_ERR_NO_DEVICE", 7: "FATTN_ERR_INTERNAL"}
+UNFUSED_STATIC_BYTES = 64 << 20  # FATTN_UNFUSED_STATIC_BYTES
 PLAN_FIELDS = ("path", "grid_x", "grid_y", "threads", "smem_bytes", "tasks", "kv_tiles",
                "rows_per_task", "keys_per_kv_tile")
 
@@ -67,6 +69,7 @@ def load():
                                    i64, i64, i64, i64, f32, ci, ci, vp]
     lib.fattn_fwd_unfused.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, ci,
                                       ci, vp]
+    lib.fattn_fwd_unfused_static.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, ci, ci, vp]
     lib.fattn_unfused_workspace_bytes.argtypes = [i64, i64, i64]
     lib.fattn_unfused_workspace_bytes.restype = i64
     lib.fattn_plan.argtypes = [i64, i64, i64, i64, ci, ci, ci, ctypes.POINTER(i64)]
@@ -75,7 +78,8 @@ def load():
     lib.fattn_status_string.argtypes = [ci]
     lib.fattn_status_string.restype = ctypes.c_char_p
     lib.fattn_version.argtypes = []
-    for f in ("fattn_fwd", "fattn_fwd_gqa", "fattn_fwd_host", "fattn_fwd_unfused", "fattn_plan", "fattn_get_device_status",
+    for f in ("fattn_fwd", "fattn_fwd_gqa", "fattn_fwd_host", "fattn_fwd_unfused",
+              "fattn_fwd_unfused_static", "fattn_plan", "fattn_get_device_status",
               "fattn_selftest_wait_timeout", "fattn_version"):
         getattr(lib, f).restype = ci
     _lib = lib
@@ -215,6 +219,31 @@ def fwd_unfused(q, k, v, causal=False, scale=None, out=None, lse=None, workspace
                                    float(scale), int(bool(causal)), DTYPE_CODES[q.dtype],
                                    _stream_handle(stream))
     _check(rc, "fattn_fwd_unfused")
+    return out, (lse if return_lse else None)
+
+
+def fwd_unfused_static(q, k, v, causal=False, scale=None, out=None, lse=None, return_lse=True,
+                       stream=None):
+    """``fwd_unfused`` with the library's fixed per-device workspace of
+    UNFUSED_STATIC_BYTES (no workspace argument, nothing allocated by the
+    library).  Calls on one device must not overlap in time (one stream)."""
+    _check_qkv(q, k, v)
+    if not q.is_cuda:
+        raise ValueError("fwd_unfused_static needs CUDA tensors")
+    B, H, N, D = q.shape
+    if scale is None:
+        scale = _default_scale(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    lse_ptr = lse.data_ptr() if (return_lse and lse is not None) else None
+    lib = load()
+    with torch.cuda.device(q.device):
+        rc = lib.fattn_fwd_unfused_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                          lse_ptr, B, H, N, D, float(scale), int(bool(causal)),
+                                          DTYPE_CODES[q.dtype], _stream_handle(stream))
+    _check(rc, "fattn_fwd_unfused_static")
     return out, (lse if return_lse else None)
 
 

@@ -350,6 +350,24 @@ int fattn_fwd_unfused(const void* q, const void* k, const void* v, void* o, floa
     return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
+int fattn_fwd_unfused_static(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal,
+                             int dtype, fattn_stream_t stream_h) {
+    bool empty = false;
+    int st = validate(q, k, v, o, lse, B, H, H, N, D, scale, dtype, &empty);
+    if (st != FATTN_OK || empty) return st;
+    if (dtype == FATTN_F32) return FATTN_ERR_UNSUPPORTED;
+    const int64_t need = fattn_unfused_workspace_bytes(B, H, N);
+    if (need <= 0 || need > static_cast<int64_t>(kUnfusedStaticBytes)) return FATTN_ERR_UNSUPPORTED;
+    int sms = 0;
+    st = current_sm_count(&sms);
+    if (st != FATTN_OK) return st;
+    void* scratch = nullptr;
+    if (unfused_static_scratch(&scratch) != cudaSuccess) return FATTN_ERR_CUDA;
+    return fattn_fwd_unfused(q, k, v, o, lse, scratch, static_cast<int64_t>(kUnfusedStaticBytes), B, H,
+                             N, D, scale, causal, dtype, stream_h);
+}
+
 int fattn_get_device_status(fattn_stream_t stream_h) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FATTN_ERR_CUDA;

@@ -16,6 +16,7 @@
 // keys in that range).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <mutex>
 
 #include "internal.h"
 #include "sm103_ptx.cuh"
@@ -431,6 +432,31 @@ cudaError_t launch_all(const UnfusedArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+// Fixed workspace of fattn_fwd_unfused_static: one array per device, in the
+// module's static device memory, so that the call allocates nothing.  Every
+// element a call reads is written earlier in the same call, so nothing in it
+// has to start at zero.
+static __device__ __align__(256) uint8_t g_unfused_static_scratch[kUnfusedStaticBytes];
+
+cudaError_t unfused_static_scratch(void** ptr) {
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        e = cudaGetSymbolAddress(&addr[dev], g_unfused_static_scratch);
+        if (e != cudaSuccess) {
+            addr[dev] = nullptr;
+            return e;
+        }
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
+}
 
 cudaError_t unfused_read_and_clear_error_word(uint32_t* out) {
     uint32_t v = 0;

@@ -72,6 +72,10 @@ size_t unfused_workspace_bytes(int64_t BH, int64_t N);
 cudaError_t unfused_encode_p_map(UnfusedArgs& a, int64_t BH, int64_t N, bool bf16);
 cudaError_t unfused_launch(const UnfusedArgs& a, int D, bool bf16, bool causal, cudaStream_t s);
 cudaError_t unfused_read_and_clear_error_word(uint32_t* out);
+// Device address of the fixed workspace of fattn_fwd_unfused_static on the
+// current device (looked up once per device).
+constexpr size_t kUnfusedStaticBytes = size_t(64) << 20;
+cudaError_t unfused_static_scratch(void** ptr);
 
 // Key/value head read by query head bh = b*H + h: b*Hkv + h / (H/Hkv).
 __host__ __device__ __forceinline__ int kv_head_of(int bh, int H, int Hkv) {
