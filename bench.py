@@ -55,9 +55,10 @@ METRIC = "attn fwd TFLOP/s (B=4,H=16,N=4096,D=128 bf16) and % of GB300 BF16 peak
 # while the sources still hash the same; null once the kernel has changed.
 KERNEL_SOURCES = ["fwd_tc.cu", "fwd_ffma.cu", "sm103_ptx.cuh", "internal.h", "fattn_api.cu"]
 NCU_TRAFFIC = {
-    "bf16_B4_H16_N4096_D128": (201420288 + 37305088, "05970775ad5b4aaf"),
-    "bf16_B2_H32_N8192_D128_causal_qstd4": (2468442000 + 128103936, "05970775ad5b4aaf"),
-    "fp16_B1_H16_N16000_D64_causal": (127311616 + 14989568, "05970775ad5b4aaf"),
+    "bf16_B4_H16_N4096_D128": (201617152 + 35978240, "d772e6e854ec039e"),
+    "bf16_B2_H32_N8192_D128_causal_qstd4": (2664641536 + 126893056, "d772e6e854ec039e"),
+    "fp16_B1_H16_N16000_D64_causal": (124670976 + 13032448, "d772e6e854ec039e"),
+    "fp32_B4_H8_N8192_D64_causal": (202038528 + 52068352, "d772e6e854ec039e"),
 }
 
 
