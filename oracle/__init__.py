@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for exact scaled-dot-product attention forward.
+"""fp64 CPU oracle for exact scaled-dot-product attention (forward and backward).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 benchmark's ``cpu_baseline`` / ``--impl reference`` legs may import this
@@ -53,10 +53,21 @@ class OracleLib:
                                             ctypes.c_double, ci, ci]
         lib.attn_oracle_rows_gqa.argtypes = [dp, dp, dp, i64, i64, i64, i64, i64,
                                              ctypes.c_double, ci, i64p, i64p, i64, dp, dp, ci]
+        lib.attn_oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64,
+                                        ctypes.c_double, ci, ci]
+        lib.attn_oracle_bwd_stats.argtypes = [dp, dp, dp, dp, i64, i64, i64, i64,
+                                              ctypes.c_double, ci, i64p, i64, dp, dp, ci]
+        lib.attn_oracle_bwd_dq_rows.argtypes = [dp, dp, dp, dp, i64, i64, i64, i64,
+                                                ctypes.c_double, ci, i64p, i64, dp, dp,
+                                                i64p, i64p, i64, dp, ci]
+        lib.attn_oracle_bwd_dkdv_rows.argtypes = [dp, dp, dp, dp, i64, i64, i64, i64,
+                                                  ctypes.c_double, ci, i64p, i64, dp, dp,
+                                                  i64p, i64p, i64, dp, dp, ci]
         lib.attn_oracle_default_threads.argtypes = []
         for f in ("attn_oracle_fwd", "attn_oracle_rows", "attn_oracle_probs",
                   "attn_oracle_online_fwd", "attn_oracle_fwd_gqa", "attn_oracle_rows_gqa",
-                  "attn_oracle_default_threads"):
+                  "attn_oracle_bwd", "attn_oracle_bwd_stats", "attn_oracle_bwd_dq_rows",
+                  "attn_oracle_bwd_dkdv_rows", "attn_oracle_default_threads"):
             getattr(lib, f).restype = ci
         self._lib = lib
         self.path = path
@@ -159,6 +170,61 @@ class OracleLib:
             raise RuntimeError("attn_oracle_online_fwd failed: %d" % rc)
         return o, lse
 
+    def backward(self, q, k, v, dout, scale, causal=False, nthreads=0):
+        """Gradients of sum(dout * O) from the definition.  Returns (dq, dk, dv) fp64."""
+        q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
+        B, H, N, D = _check4(q, k, v)
+        if do.shape != q.shape:
+            raise ValueError("dout must have q's shape")
+        dq, dk, dv = (np.full((B, H, N, D), np.nan, np.float64) for _ in range(3))
+        rc = self._lib.attn_oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk),
+                                       _ptr(dv), B, H, N, D, float(scale), int(bool(causal)),
+                                       int(nthreads))
+        if rc != 0:
+            raise RuntimeError("attn_oracle_bwd failed: %d" % rc)
+        return dq, dk, dv
+
+    def backward_rows(self, q, k, v, dout, scale, causal, bh_rows, rows, bh_keys, keys,
+                      nthreads=0):
+        """Selected rows of dQ (heads bh_rows, query rows `rows`) and of dK, dV
+        (heads bh_keys, keys `keys`).  Returns (dq [R,D], dk [K,D], dv [K,D])."""
+        q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
+        B, H, N, D = _check4(q, k, v)
+        if do.shape != q.shape:
+            raise ValueError("dout must have q's shape")
+        bh_rows = np.asarray(bh_rows, np.int64).ravel()
+        bh_keys = np.asarray(bh_keys, np.int64).ravel()
+        rows = np.ascontiguousarray(np.asarray(rows, np.int64).ravel())
+        keys = np.ascontiguousarray(np.asarray(keys, np.int64).ravel())
+        if bh_rows.shape != rows.shape or bh_keys.shape != keys.shape:
+            raise ValueError("head and index lists must have equal lengths")
+        heads = np.ascontiguousarray(np.unique(np.concatenate([bh_rows, bh_keys])))
+        slot_rows = np.ascontiguousarray(np.searchsorted(heads, bh_rows).astype(np.int64))
+        slot_keys = np.ascontiguousarray(np.searchsorted(heads, bh_keys).astype(np.int64))
+        nh = heads.shape[0]
+        lse = np.empty((nh, N), np.float64)
+        delta = np.empty((nh, N), np.float64)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        ip = lambda a: a.ctypes.data_as(i64p)
+        common = (_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, H, N, D, float(scale),
+                  int(bool(causal)), ip(heads), nh)
+        rc = self._lib.attn_oracle_bwd_stats(*common, _ptr(lse), _ptr(delta), int(nthreads))
+        if rc != 0:
+            raise RuntimeError("attn_oracle_bwd_stats failed: %d" % rc)
+        dq = np.empty((rows.shape[0], D), np.float64)
+        dk = np.empty((keys.shape[0], D), np.float64)
+        dv = np.empty((keys.shape[0], D), np.float64)
+        rc = self._lib.attn_oracle_bwd_dq_rows(*common, _ptr(lse), _ptr(delta), ip(slot_rows),
+                                               ip(rows), rows.shape[0], _ptr(dq), int(nthreads))
+        if rc != 0:
+            raise RuntimeError("attn_oracle_bwd_dq_rows failed: %d" % rc)
+        rc = self._lib.attn_oracle_bwd_dkdv_rows(*common, _ptr(lse), _ptr(delta), ip(slot_keys),
+                                                 ip(keys), keys.shape[0], _ptr(dk), _ptr(dv),
+                                                 int(nthreads))
+        if rc != 0:
+            raise RuntimeError("attn_oracle_bwd_dkdv_rows failed: %d" % rc)
+        return dq, dk, dv
+
 
 _default = None
 
@@ -198,10 +264,20 @@ def attention_online(q, k, v, scale, causal=False, Br=128, Bc=32, nthreads=0):
     return _get().attention_online(q, k, v, scale, causal, Br, Bc, nthreads)
 
 
+def backward(q, k, v, dout, scale, causal=False, nthreads=0):
+    return _get().backward(q, k, v, dout, scale, causal, nthreads)
+
+
+def backward_rows(q, k, v, dout, scale, causal, bh_rows, rows, bh_keys, keys, nthreads=0):
+    return _get().backward_rows(q, k, v, dout, scale, causal, bh_rows, rows, bh_keys, keys,
+                                nthreads)
+
+
 def lib_path() -> str:
     return _build.LIB
 
 
 __all__ = ["OracleLib", "attention", "attention_rows", "probabilities",
-           "attention_online", "attention_gqa", "attention_rows_gqa", "default_threads",
+           "attention_online", "attention_gqa", "attention_rows_gqa", "backward",
+           "backward_rows", "default_threads",
            "lib_path"]

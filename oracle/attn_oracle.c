@@ -394,3 +394,297 @@ int attn_oracle_online_fwd(const double* q, const double* k, const double* v,
     free(tid); free(jobs); free(started);
     return rc;
 }
+
+/* ===========================================================================
+ * Backward pass: the gradients of L = sum_{i,c} dO_ic * O_ic with respect to
+ * Q, K and V, for a given upstream gradient dO.
+ *
+ * The chang-wenbin.github.io FA2 report (section "反向传播性能分析") only
+ * sketches the backward kernel (the forward's tiling, gradient buffers
+ * updated in place with atomics).  The gradients themselves are the chain
+ * rule through the definition used by one_row above, written out per
+ * element:
+ *   P_ij    = exp(s_ij - LSE_i)            for visible j, s_ij = scale q_i.k_j
+ *   dV_j    = sum_i P_ij dO_i
+ *   dP_ij   = dO_i . v_j
+ *   Delta_i = sum_j P_ij dP_ij              (= dO_i . O_i)
+ *   dS_ij   = P_ij (dP_ij - Delta_i)       (softmax Jacobian)
+ *   dQ_i    = scale sum_j dS_ij k_j
+ *   dK_j    = scale sum_i dS_ij q_i
+ * Sums run over the visible pairs only (j <= i under causal masking).
+ * ========================================================================= */
+
+/* LSE_i and Delta_i of row i of one head.  s: scratch of N doubles. */
+static void bwd_row_stats(const double* qh, const double* kh, const double* vh,
+                          const double* doh, int64_t N, int64_t D, double scale,
+                          int causal, int64_t i, double* s,
+                          double* lse_out, double* delta_out)
+{
+    const double* qi = qh + i * D;
+    const double* doi = doh + i * D;
+    int64_t nvis = causal ? (i + 1) : N;
+    if (nvis > N) nvis = N;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nvis; ++j) {
+        const double* kj = kh + j * D;
+        double dot = 0.0;
+        for (int64_t d = 0; d < D; ++d) dot += qi[d] * kj[d];
+        s[j] = scale * dot;
+        if (s[j] > m) m = s[j];
+    }
+    double z = 0.0;
+    for (int64_t j = 0; j < nvis; ++j) z += exp(s[j] - m);
+    const double lse = m + log(z);
+    double delta = 0.0;
+    for (int64_t j = 0; j < nvis; ++j) {
+        const double* vj = vh + j * D;
+        double dp = 0.0;
+        for (int64_t c = 0; c < D; ++c) dp += doi[c] * vj[c];
+        delta += exp(s[j] - lse) * dp;
+    }
+    *lse_out = lse;
+    *delta_out = delta;
+}
+
+/* dQ_i = scale sum_j P_ij (dP_ij - Delta_i) k_j */
+static void bwd_dq_row(const double* qh, const double* kh, const double* vh,
+                       const double* doh, int64_t N, int64_t D, double scale,
+                       int causal, int64_t i, double lse_i, double delta_i,
+                       double* dq_row)
+{
+    const double* qi = qh + i * D;
+    const double* doi = doh + i * D;
+    int64_t nvis = causal ? (i + 1) : N;
+    if (nvis > N) nvis = N;
+    for (int64_t c = 0; c < D; ++c) dq_row[c] = 0.0;
+    for (int64_t j = 0; j < nvis; ++j) {
+        const double* kj = kh + j * D;
+        const double* vj = vh + j * D;
+        double dot = 0.0, dp = 0.0;
+        for (int64_t d = 0; d < D; ++d) dot += qi[d] * kj[d];
+        for (int64_t c = 0; c < D; ++c) dp += doi[c] * vj[c];
+        const double p = exp(scale * dot - lse_i);
+        const double ds = p * (dp - delta_i);
+        for (int64_t c = 0; c < D; ++c) dq_row[c] += scale * ds * kj[c];
+    }
+}
+
+/* dK_j = scale sum_i P_ij (dP_ij - Delta_i) q_i and dV_j = sum_i P_ij dO_i,
+ * over the rows i that see key j (i >= j under causal masking). */
+static void bwd_dkdv_row(const double* qh, const double* kh, const double* vh,
+                         const double* doh, int64_t N, int64_t D, double scale,
+                         int causal, int64_t j, const double* lse_h,
+                         const double* delta_h, double* dk_row, double* dv_row)
+{
+    const double* kj = kh + j * D;
+    const double* vj = vh + j * D;
+    for (int64_t c = 0; c < D; ++c) { dk_row[c] = 0.0; dv_row[c] = 0.0; }
+    for (int64_t i = causal ? j : 0; i < N; ++i) {
+        const double* qi = qh + i * D;
+        const double* doi = doh + i * D;
+        double dot = 0.0, dp = 0.0;
+        for (int64_t d = 0; d < D; ++d) dot += qi[d] * kj[d];
+        for (int64_t c = 0; c < D; ++c) dp += doi[c] * vj[c];
+        const double p = exp(scale * dot - lse_h[i]);
+        const double ds = p * (dp - delta_h[i]);
+        for (int64_t c = 0; c < D; ++c) {
+            dv_row[c] += p * doi[c];
+            dk_row[c] += scale * ds * qi[c];
+        }
+    }
+}
+
+/* Generic split of nitems independent items over threads (contiguous chunks),
+ * each thread with its own scratch of `scratch_len` doubles. */
+typedef void (*item_fn)(const void* ctx, int64_t item, double* scratch);
+
+typedef struct {
+    item_fn fn;
+    const void* ctx;
+    int64_t begin, end, scratch_len;
+    int failed;
+} item_job;
+
+static void* item_worker(void* arg)
+{
+    item_job* jb = (item_job*)arg;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(jb->scratch_len > 0 ? jb->scratch_len : 1));
+    if (!s) { jb->failed = 1; return NULL; }
+    for (int64_t it = jb->begin; it < jb->end; ++it) jb->fn(jb->ctx, it, s);
+    free(s);
+    return NULL;
+}
+
+static int parallel_items(item_fn fn, const void* ctx, int64_t nitems, int64_t scratch_len,
+                          int nthreads)
+{
+    if (nitems <= 0) return 0;
+    int nt = resolve_threads(nthreads);
+    if (nt > nitems) nt = (int)nitems;
+    pthread_t* tid = (pthread_t*)calloc((size_t)nt, sizeof(pthread_t));
+    item_job* jobs = (item_job*)calloc((size_t)nt, sizeof(item_job));
+    int* started = (int*)calloc((size_t)nt, sizeof(int));
+    if (!tid || !jobs || !started) { free(tid); free(jobs); free(started); return -3; }
+    int rc = 0;
+    for (int t = 0; t < nt; ++t) {
+        jobs[t].fn = fn;
+        jobs[t].ctx = ctx;
+        jobs[t].begin = nitems * t / nt;
+        jobs[t].end = nitems * (t + 1) / nt;
+        jobs[t].scratch_len = scratch_len;
+        if (nt == 1) {
+            item_worker(&jobs[t]);
+        } else if (pthread_create(&tid[t], NULL, item_worker, &jobs[t]) == 0) {
+            started[t] = 1;
+        } else {
+            item_worker(&jobs[t]);
+        }
+    }
+    for (int t = 0; t < nt; ++t) {
+        if (started[t]) pthread_join(tid[t], NULL);
+        if (jobs[t].failed) rc = -3;
+    }
+    free(tid); free(jobs); free(started);
+    return rc;
+}
+
+typedef struct {
+    const double *q, *k, *v, *dout;
+    int64_t N, D;
+    double scale;
+    int causal;
+    const int64_t* heads;            /* head (b*H + h) of each slot */
+    double *lse, *delta;             /* [nslots][N] */
+    const double *lse_c, *delta_c;   /* read-only views of the same */
+    const int64_t *slot_idx, *idx;   /* requests: slot and row (or key) */
+    double *out0, *out1;             /* dq rows, or dk and dv rows */
+} bwd_ctx;
+
+static void stats_item(const void* vctx, int64_t it, double* s)
+{
+    const bwd_ctx* c = (const bwd_ctx*)vctx;
+    const int64_t slot = it / c->N, i = it % c->N;
+    const int64_t head = c->heads[slot] * c->N * c->D;
+    bwd_row_stats(c->q + head, c->k + head, c->v + head, c->dout + head, c->N, c->D,
+                  c->scale, c->causal, i, s, c->lse + it, c->delta + it);
+}
+
+static void dq_item(const void* vctx, int64_t it, double* s)
+{
+    const bwd_ctx* c = (const bwd_ctx*)vctx;
+    (void)s;
+    const int64_t slot = c->slot_idx[it], i = c->idx[it];
+    const int64_t head = c->heads[slot] * c->N * c->D;
+    bwd_dq_row(c->q + head, c->k + head, c->v + head, c->dout + head, c->N, c->D,
+               c->scale, c->causal, i, c->lse_c[slot * c->N + i],
+               c->delta_c[slot * c->N + i], c->out0 + it * c->D);
+}
+
+static void dkdv_item(const void* vctx, int64_t it, double* s)
+{
+    const bwd_ctx* c = (const bwd_ctx*)vctx;
+    (void)s;
+    const int64_t slot = c->slot_idx[it], j = c->idx[it];
+    const int64_t head = c->heads[slot] * c->N * c->D;
+    bwd_dkdv_row(c->q + head, c->k + head, c->v + head, c->dout + head, c->N, c->D,
+                 c->scale, c->causal, j, c->lse_c + slot * c->N, c->delta_c + slot * c->N,
+                 c->out0 + it * c->D, c->out1 + it * c->D);
+}
+
+int attn_oracle_bwd_stats(const double* q, const double* k, const double* v,
+                          const double* dout, int64_t B, int64_t H, int64_t N, int64_t D,
+                          double scale, int causal, const int64_t* heads, int64_t nheads,
+                          double* lse, double* delta, int nthreads)
+{
+    if (check_shape(B, H, N, D) || nheads < 0) return -1;
+    if (nheads == 0 || N == 0) return 0;
+    if (!q || !k || !v || !dout || !heads || !lse || !delta) return -2;
+    for (int64_t t = 0; t < nheads; ++t)
+        if (heads[t] < 0 || heads[t] >= B * H) return -1;
+    bwd_ctx c;
+    memset(&c, 0, sizeof(c));
+    c.q = q; c.k = k; c.v = v; c.dout = dout;
+    c.N = N; c.D = D; c.scale = scale; c.causal = causal;
+    c.heads = heads; c.lse = lse; c.delta = delta;
+    return parallel_items(stats_item, &c, nheads * N, N, nthreads);
+}
+
+int attn_oracle_bwd_dq_rows(const double* q, const double* k, const double* v,
+                            const double* dout, int64_t B, int64_t H, int64_t N, int64_t D,
+                            double scale, int causal, const int64_t* heads, int64_t nheads,
+                            const double* lse, const double* delta,
+                            const int64_t* slot_idx, const int64_t* row_idx, int64_t nrows,
+                            double* dq_rows, int nthreads)
+{
+    if (check_shape(B, H, N, D) || nheads < 0 || nrows < 0) return -1;
+    if (nrows == 0) return 0;
+    if (!q || !k || !v || !dout || !heads || !lse || !delta || !slot_idx || !row_idx || !dq_rows)
+        return -2;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (slot_idx[r] < 0 || slot_idx[r] >= nheads || row_idx[r] < 0 || row_idx[r] >= N) return -1;
+    for (int64_t t = 0; t < nheads; ++t)
+        if (heads[t] < 0 || heads[t] >= B * H) return -1;
+    bwd_ctx c;
+    memset(&c, 0, sizeof(c));
+    c.q = q; c.k = k; c.v = v; c.dout = dout;
+    c.N = N; c.D = D; c.scale = scale; c.causal = causal;
+    c.heads = heads; c.lse_c = lse; c.delta_c = delta;
+    c.slot_idx = slot_idx; c.idx = row_idx; c.out0 = dq_rows;
+    return parallel_items(dq_item, &c, nrows, 1, nthreads);
+}
+
+int attn_oracle_bwd_dkdv_rows(const double* q, const double* k, const double* v,
+                              const double* dout, int64_t B, int64_t H, int64_t N, int64_t D,
+                              double scale, int causal, const int64_t* heads, int64_t nheads,
+                              const double* lse, const double* delta,
+                              const int64_t* slot_idx, const int64_t* key_idx, int64_t nkeys,
+                              double* dk_rows, double* dv_rows, int nthreads)
+{
+    if (check_shape(B, H, N, D) || nheads < 0 || nkeys < 0) return -1;
+    if (nkeys == 0) return 0;
+    if (!q || !k || !v || !dout || !heads || !lse || !delta || !slot_idx || !key_idx ||
+        !dk_rows || !dv_rows)
+        return -2;
+    for (int64_t r = 0; r < nkeys; ++r)
+        if (slot_idx[r] < 0 || slot_idx[r] >= nheads || key_idx[r] < 0 || key_idx[r] >= N) return -1;
+    for (int64_t t = 0; t < nheads; ++t)
+        if (heads[t] < 0 || heads[t] >= B * H) return -1;
+    bwd_ctx c;
+    memset(&c, 0, sizeof(c));
+    c.q = q; c.k = k; c.v = v; c.dout = dout;
+    c.N = N; c.D = D; c.scale = scale; c.causal = causal;
+    c.heads = heads; c.lse_c = lse; c.delta_c = delta;
+    c.slot_idx = slot_idx; c.idx = key_idx; c.out0 = dk_rows; c.out1 = dv_rows;
+    return parallel_items(dkdv_item, &c, nkeys, 1, nthreads);
+}
+
+int attn_oracle_bwd(const double* q, const double* k, const double* v, const double* dout,
+                    double* dq, double* dk, double* dv,
+                    int64_t B, int64_t H, int64_t N, int64_t D,
+                    double scale, int causal, int nthreads)
+{
+    if (check_shape(B, H, N, D)) return -1;
+    const int64_t BH = B * H;
+    if (BH * N == 0) return 0;
+    if (!q || !k || !v || !dout || !dq || !dk || !dv) return -2;
+    int64_t* heads = (int64_t*)malloc(sizeof(int64_t) * (size_t)BH);
+    int64_t* slot = (int64_t*)malloc(sizeof(int64_t) * (size_t)(BH * N));
+    int64_t* idx = (int64_t*)malloc(sizeof(int64_t) * (size_t)(BH * N));
+    double* lse = (double*)malloc(sizeof(double) * (size_t)(BH * N));
+    double* delta = (double*)malloc(sizeof(double) * (size_t)(BH * N));
+    int rc = -3;
+    if (heads && slot && idx && lse && delta) {
+        for (int64_t t = 0; t < BH; ++t) heads[t] = t;
+        for (int64_t it = 0; it < BH * N; ++it) { slot[it] = it / N; idx[it] = it % N; }
+        rc = attn_oracle_bwd_stats(q, k, v, dout, B, H, N, D, scale, causal, heads, BH,
+                                   lse, delta, nthreads);
+        if (rc == 0)
+            rc = attn_oracle_bwd_dq_rows(q, k, v, dout, B, H, N, D, scale, causal, heads, BH,
+                                         lse, delta, slot, idx, BH * N, dq, nthreads);
+        if (rc == 0)
+            rc = attn_oracle_bwd_dkdv_rows(q, k, v, dout, B, H, N, D, scale, causal, heads, BH,
+                                           lse, delta, slot, idx, BH * N, dk, dv, nthreads);
+    }
+    free(heads); free(slot); free(idx); free(lse); free(delta);
+    return rc;
+}

@@ -96,6 +96,43 @@ int attn_oracle_rows_gqa(const double* q, const double* k, const double* v,
                          const int64_t* bh_idx, const int64_t* row_idx, int64_t nrows,
                          double* o_rows, double* lse_rows, int nthreads);
 
+/* ---- backward pass ------------------------------------------------------
+ * Gradients of L = sum dO * O with respect to Q, K, V for the upstream
+ * gradient dout ([B,H,N,D]), from the chain rule through the definition:
+ * dV_j = sum_i P_ij dO_i; dP_ij = dO_i.v_j; Delta_i = sum_j P_ij dP_ij;
+ * dS_ij = P_ij (dP_ij - Delta_i); dQ_i = scale sum_j dS_ij k_j;
+ * dK_j = scale sum_i dS_ij q_i (visible pairs only).  The FA2 report of
+ * chang-wenbin.github.io sketches the backward kernel without formulas.
+ * Multi-head only (k and v have q's shape). */
+int attn_oracle_bwd(const double* q, const double* k, const double* v, const double* dout,
+                    double* dq, double* dk, double* dv,
+                    int64_t B, int64_t H, int64_t N, int64_t D,
+                    double scale, int causal, int nthreads);
+
+/* Per-row LSE_i and Delta_i of the heads listed in heads[0..nheads) (each a
+ * b*H + h index); lse and delta are [nheads][N]. */
+int attn_oracle_bwd_stats(const double* q, const double* k, const double* v,
+                          const double* dout, int64_t B, int64_t H, int64_t N, int64_t D,
+                          double scale, int causal, const int64_t* heads, int64_t nheads,
+                          double* lse, double* delta, int nthreads);
+
+/* Selected rows of dQ: request r is row row_idx[r] of head heads[slot_idx[r]];
+ * lse / delta as returned by attn_oracle_bwd_stats for the same heads list. */
+int attn_oracle_bwd_dq_rows(const double* q, const double* k, const double* v,
+                            const double* dout, int64_t B, int64_t H, int64_t N, int64_t D,
+                            double scale, int causal, const int64_t* heads, int64_t nheads,
+                            const double* lse, const double* delta,
+                            const int64_t* slot_idx, const int64_t* row_idx, int64_t nrows,
+                            double* dq_rows, int nthreads);
+
+/* Selected rows of dK and dV (key key_idx[r] of head heads[slot_idx[r]]). */
+int attn_oracle_bwd_dkdv_rows(const double* q, const double* k, const double* v,
+                              const double* dout, int64_t B, int64_t H, int64_t N, int64_t D,
+                              double scale, int causal, const int64_t* heads, int64_t nheads,
+                              const double* lse, const double* delta,
+                              const int64_t* slot_idx, const int64_t* key_idx, int64_t nkeys,
+                              double* dk_rows, double* dv_rows, int nthreads);
+
 /* Number of threads nthreads<=0 resolves to (CPUs in the affinity mask). */
 int attn_oracle_default_threads(void);
 

@@ -280,7 +280,99 @@ def pin_gqa_bruteforce(orc):
             _close(lse[:, h:h + 1], lb, 1e-13, "gqa brute lse")
 
 
+# ---------------------------------------------------------------------------
+# Backward pass.  The pages give no formulas (the FA2 report only sketches the
+# kernel), so the gradients are pinned to the forward definition itself by
+# central finite differences, and to closed forms that follow from softmax
+# rows summing to one.
+# ---------------------------------------------------------------------------
+def _loss(orc, q, k, v, dout, scale, causal):
+    o, _ = orc.attention(q, k, v, scale, causal)
+    return float(np.sum(o * dout))
+
+
+def pin_bwd_finite_differences(orc):
+    """dQ, dK, dV equal the central differences of L = sum(dO * O(Q, K, V))
+    computed with the forward oracle (step 1e-6, error O(h^2) + rounding)."""
+    r = _rng(41)
+    for (N, D, causal) in ((5, 3, False), (6, 2, True), (1, 2, True)):
+        q, k, v, do = (r.standard_normal((1, 2, N, D)) for _ in range(4))
+        scale = 0.8
+        grads = orc.backward(q, k, v, do, scale, causal)
+        h = 1e-6
+        for t, (x, g) in enumerate(zip((q, k, v), grads)):
+            for idx in np.ndindex(x.shape):
+                args = [q, k, v]
+                xp = x.copy()
+                xp[idx] += h
+                xm = x.copy()
+                xm[idx] -= h
+                args[t] = xp
+                lp = _loss(orc, *args, do, scale, causal)
+                args[t] = xm
+                lm = _loss(orc, *args, do, scale, causal)
+                fd = (lp - lm) / (2 * h)
+                assert abs(fd - g[idx]) <= 1e-7 * (1 + abs(fd)), \
+                    ("finite differences", "qkv"[t], idx, causal, fd, g[idx])
+
+
+def pin_bwd_closed_forms(orc):
+    """N = 1: O = V, so dV = dO and dQ = dK = 0.  dO = 0: every gradient is 0.
+    Equal value rows: O = v for every row whatever Q and K, so dQ = dK = 0 and
+    the dV rows sum to the dO rows' sum (each P row sums to 1)."""
+    r = _rng(42)
+    q, k, v, do = (r.standard_normal((2, 3, 1, 4)) for _ in range(4))
+    for causal in (False, True):
+        dq, dk, dv = orc.backward(q, k, v, do, 0.5, causal)
+        _close(dv, do, 1e-15, "N=1 dV")
+        _close(dq, np.zeros_like(dq), 1e-15, "N=1 dQ")
+        _close(dk, np.zeros_like(dk), 1e-15, "N=1 dK")
+    q, k, v = (r.standard_normal((1, 2, 9, 4)) for _ in range(3))
+    for causal in (False, True):
+        grads = orc.backward(q, k, v, np.zeros_like(q), 0.5, causal)
+        for g in grads:
+            _close(g, np.zeros_like(g), 0.0, "dO = 0")
+    vconst = np.broadcast_to(r.standard_normal((1, 2, 1, 4)), (1, 2, 9, 4)).copy()
+    do = r.standard_normal((1, 2, 9, 4))
+    for causal in (False, True):
+        dq, dk, dv = orc.backward(q, k, vconst, do, 0.5, causal)
+        _close(dq, np.zeros_like(dq), 1e-13, "constant V dQ")
+        _close(dk, np.zeros_like(dk), 1e-13, "constant V dK")
+        _close(dv.sum(axis=2), do.sum(axis=2), 1e-12, "constant V sum dV")
+
+
+def pin_bwd_invariances(orc):
+    """Shifting every key by one vector u changes each score row by a constant,
+    so O and every gradient are unchanged; and since each row of dS sums to
+    zero, the key gradients of a head sum to zero."""
+    r = _rng(43)
+    q, k, v, do = (r.standard_normal((2, 2, 13, 5)) for _ in range(4))
+    u = r.standard_normal((1, 1, 1, 5))
+    for causal in (False, True):
+        g0 = orc.backward(q, k, v, do, 0.6, causal)
+        g1 = orc.backward(q, k + u, v, do, 0.6, causal)
+        for a, b, n in zip(g0, g1, ("dQ", "dK", "dV")):
+            _close(a, b, 1e-12, "key shift " + n)
+        _close(g0[1].sum(axis=2), np.zeros((2, 2, 5)), 1e-12, "sum_j dK_j")
+
+
+def pin_bwd_rows_match_full(orc):
+    r = _rng(44)
+    B, H, N, D = 2, 2, 19, 6
+    q, k, v, do = (r.standard_normal((B, H, N, D)) for _ in range(4))
+    for causal in (False, True):
+        dq, dk, dv = orc.backward(q, k, v, do, 0.4, causal)
+        bh_r, rows = r.integers(0, B * H, 11), r.integers(0, N, 11)
+        bh_k, keys = r.integers(0, B * H, 9), r.integers(0, N, 9)
+        sq, sk, sv = orc.backward_rows(q, k, v, do, 0.4, causal, bh_r, rows, bh_k, keys)
+        _close(sq, dq.reshape(B * H, N, D)[bh_r, rows], 0.0, "rows dQ")
+        _close(sk, dk.reshape(B * H, N, D)[bh_k, keys], 0.0, "rows dK")
+        _close(sv, dv.reshape(B * H, N, D)[bh_k, keys], 0.0, "rows dV")
+
+
 ALL_PINS = [pin_row_sums, pin_ones_v, pin_zero_q, pin_basis_v, pin_shift_invariance,
             pin_single_key, pin_causal_first_rows, pin_permutation, pin_bruteforce,
             pin_rows_match_full, pin_online_matches_definition, pin_golden_dot,
-            pin_golden_max_row, pin_gqa_equals_repeated_heads, pin_gqa_bruteforce]
+            pin_golden_max_row, pin_gqa_equals_repeated_heads, pin_gqa_bruteforce,
+            pin_bwd_finite_differences, pin_bwd_closed_forms, pin_bwd_invariances,
+            pin_bwd_rows_match_full]

@@ -47,6 +47,19 @@ MUTANTS = [
     ("online_l_not_rescaled", "l[r] = corr * l[r] + lsum;", "l[r] = l[r] + lsum;"),
     ("gqa_interleaved_heads", "const int64_t kvh = b * jb->Hkv + h / (jb->H / jb->Hkv);",
      "const int64_t kvh = b * jb->Hkv + h % jb->Hkv;"),
+    ("bwd_dk_dropped_scale", "dk_row[c] += scale * ds * qi[c];", "dk_row[c] += ds * qi[c];"),
+    ("bwd_dq_wrong_operand", "dq_row[c] += scale * ds * kj[c];", "dq_row[c] += scale * ds * qi[c];"),
+    ("bwd_ds_sign", "const double ds = p * (dp - delta_h[i]);", "const double ds = p * (delta_h[i] - dp);"),
+    ("bwd_dq_delta_dropped", "const double ds = p * (dp - delta_i);", "const double ds = p * dp;"),
+    ("bwd_delta_unweighted", "delta += exp(s[j] - lse) * dp;", "delta += dp;"),
+    ("bwd_lse_without_max", "const double lse = m + log(z);", "const double lse = log(z);"),
+    ("bwd_dv_uses_ds", "dv_row[c] += p * doi[c];", "dv_row[c] += ds * doi[c];"),
+    ("bwd_dkdv_causal_skips_diagonal", "for (int64_t i = causal ? j : 0; i < N; ++i) {",
+     "for (int64_t i = causal ? j + 1 : 0; i < N; ++i) {"),
+    ("bwd_dq_ignores_causal", "int64_t nvis = causal ? (i + 1) : N;\n    if (nvis > N) nvis = N;\n    for (int64_t c = 0; c < D; ++c) dq_row[c] = 0.0;",
+     "int64_t nvis = N;\n    if (nvis > N) nvis = N;\n    for (int64_t c = 0; c < D; ++c) dq_row[c] = 0.0;"),
+    ("bwd_dp_wrong_row", "for (int64_t c = 0; c < D; ++c) dp += doi[c] * vj[c];\n        const double p = exp(scale * dot - lse_i);",
+     "for (int64_t c = 0; c < D; ++c) dp += doh[c] * vj[c];\n        const double p = exp(scale * dot - lse_i);"),
     ("gqa_no_batch_offset", "const int64_t kvh = b * jb->Hkv + h / (jb->H / jb->Hkv);",
      "const int64_t kvh = h / (jb->H / jb->Hkv) + 0 * b;"),
 ]
