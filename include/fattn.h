@@ -130,6 +130,44 @@ FATTN_API int fattn_fwd_host(const void* q_host, const void* k_host, const void*
                    int dtype, fattn_stream_t stream);
 
 /*
+ * fattn_bwd_workspace_bytes -- bytes of device workspace fattn_bwd needs:
+ * fp32 [B*H][2][Npad] (per row LSE*log2(e) and Delta = dO.O, Npad = N
+ * rounded up to 128), i.e. 8 * B*H*Npad.  0 for an empty or invalid size.
+ */
+FATTN_API int64_t fattn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N);
+
+/*
+ * fattn_bwd -- attention backward: the gradients dQ, dK, dV of
+ * L = sum(dO * O) for O = softmax(scale * Q K^T [+ causal mask]) V, given the
+ * forward's output O and log-sum-exp LSE (as fattn_fwd writes them) and the
+ * upstream gradient dO.  The FA2 report of chang-wenbin.github.io (section
+ * "反向传播性能分析") sketches this pass: the forward's tiling, scores
+ * recomputed rather than stored.  Per visible pair: P_ij = exp(s_ij - LSE_i),
+ * dP_ij = dO_i.v_j, dS_ij = P_ij (dP_ij - Delta_i) with Delta_i = dO_i.O_i;
+ * dV_j = sum_i P_ij dO_i, dK_j = scale sum_i dS_ij q_i, dQ_i = scale sum_j
+ * dS_ij k_j.  P and dS are rounded to the input dtype before the products
+ * that consume them; every sum accumulates in fp32.
+ *
+ *   q, k, v, o, dout : device, [B,H,N,D] of `dtype`, read only, 16-byte aligned.
+ *   lse              : device, fp32 [B,H,N] (natural log), read only.
+ *   dq, dk, dv       : device, [B,H,N,D] of `dtype`, written; 16-byte aligned;
+ *                      overlapping no input and no other output.
+ *   workspace        : caller-owned device scratch of at least
+ *                      fattn_bwd_workspace_bytes(B, H, N) bytes, 16-byte
+ *                      aligned, overlapping nothing else; contents ignored.
+ *   dtype            : FATTN_BF16 or FATTN_F16 (FATTN_F32 -> FATTN_ERR_UNSUPPORTED).
+ *   B,H,N,D,scale,causal : as fattn_fwd (multi-head: k and v have q's shape).
+ *
+ * Three kernel launches on `stream` (row statistics, dK/dV, dQ); each
+ * gradient row is produced by exactly one CTA, so the result is
+ * deterministic.  Errors as fattn_fwd.
+ */
+FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, const void* o,
+              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+              void* workspace, int64_t workspace_bytes, int64_t B, int64_t H, int64_t N,
+              int64_t D, float scale, int causal, int dtype, fattn_stream_t stream);
+
+/*
  * fattn_unfused_workspace_bytes -- bytes of device workspace fattn_fwd_unfused
  * needs for B*H heads of length N: S fp32 [B*H][N][Np] followed by P 16-bit
  * [B*H][N][Np], Np = N rounded up to a multiple of 8, i.e. 6 * B*H*N*Np.

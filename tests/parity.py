@@ -73,3 +73,80 @@ def sample_rows(B, H, N, count, seed, causal):
     bh += list(r.integers(0, B * H, count))
     rows += list(r.integers(0, N, count))
     return np.asarray(bh, np.int64), np.asarray(rows, np.int64)
+
+
+# ---------------------------------------------------------------------------
+# Backward pass.  The target states no tolerance for gradients, so the bound
+# is derived from the arithmetic of the kernels, per element, from fp64
+# quantities of the inputs (never from the CUDA path):
+#   * P = exp(s - LSE) in fp32 from the forward's LSE: relative error EPS_P
+#     (covers the forward's LSE error and exp2.approx) plus the fp32
+#     accumulation of the products (one rounding per 16-deep MMA step);
+#   * P (for dV) and dS (for dK, dQ) rounded once to the input dtype:
+#     relative U = 2^-8 (bf16) / 2^-11 (fp16), plus the fp16 subnormal
+#     spacing 2^-24 absolute;
+#   * Delta = dO . O from the 16-bit O: |dDelta_i| <= U sum_c |dO_ic O_ic|;
+#   * the result rounded to the output dtype: half an ulp.
+# ---------------------------------------------------------------------------
+UNIT_ROUNDOFF = {torch.bfloat16: 2.0 ** -8, torch.float16: 2.0 ** -11}
+EPS_P = 1e-4
+
+
+def _subnormal(dtype):
+    """Half the spacing of the output dtype's subnormals (fp16 2^-25)."""
+    return 2.0 ** -25 if dtype == torch.float16 else 2.0 ** -134
+
+
+def _bwd_eps(N):
+    return EPS_P + (N / 16.0 + 8.0) * 2.0 ** -24
+
+
+def _head_terms(q, k, v, do, o, lse, scale, causal, rows, keys):
+    """P, dP, dS and Delta on rows x keys of one head (fp64; q,k,v,do,o [N,D])."""
+    s = scale * (q[rows] @ k[keys].T)
+    p = np.exp(s - lse[rows][:, None])
+    if causal:
+        p = np.where(np.asarray(keys)[None, :] <= np.asarray(rows)[:, None], p, 0.0)
+    dp = do[rows] @ v[keys].T
+    delta = np.sum(do[rows] * o[rows], axis=1)
+    ds = p * (dp - delta[:, None])
+    doo = np.sum(np.abs(do[rows]) * np.abs(o[rows]), axis=1)
+    return p, dp, ds, delta, doo
+
+
+def bwd_bound_dq(q, k, v, do, o, lse, scale, causal, rows, dtype, dq_ref):
+    """Per-element bound for dQ rows `rows` of one head ([len(rows), D])."""
+    N = q.shape[0]
+    u, eps = UNIT_ROUNDOFF[dtype], _bwd_eps(N)
+    keys = np.arange(N)
+    p, dp, ds, delta, doo = _head_terms(q, k, v, do, o, lse, scale, causal, rows, keys)
+    w = (1.05 * u + eps) * np.abs(ds) + p * (u * doo[:, None] + eps * (np.abs(dp) + np.abs(delta)[:, None])) \
+        + 2.0 ** -24 * (p > 0)
+    return scale * (w @ np.abs(k)) + half_ulp(dq_ref, dtype) + _subnormal(dtype)
+
+
+def bwd_bound_dkdv(q, k, v, do, o, lse, scale, causal, keys, dtype, dk_ref, dv_ref):
+    """Per-element bounds for dK and dV rows `keys` of one head."""
+    N = q.shape[0]
+    u, eps = UNIT_ROUNDOFF[dtype], _bwd_eps(N)
+    rows = np.arange(N)
+    p, dp, ds, delta, doo = _head_terms(q, k, v, do, o, lse, scale, causal, rows, keys)
+    wk = (1.05 * u + eps) * np.abs(ds) + p * (u * doo[:, None] + eps * (np.abs(dp) + np.abs(delta)[:, None])) \
+        + 2.0 ** -24 * (p > 0)
+    wv = (1.05 * u + eps) * p + 2.0 ** -24 * (p > 0)
+    bk = scale * (wk.T @ np.abs(q)) + half_ulp(dk_ref, dtype) + _subnormal(dtype)
+    bv = wv.T @ np.abs(do) + half_ulp(dv_ref, dtype) + _subnormal(dtype)
+    return bk, bv
+
+
+def compare_bound(got, ref, bound, what):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), "%s: non-finite" % what
+    err = np.abs(got - ref)
+    ratio = err / bound
+    worst = float(ratio.max()) if ratio.size else 0.0
+    assert worst <= 1.0, "%s: %d elements over the bound (worst err/bound %.2f, max err %.3e, max |ref| %.3e)" % (
+        what, int((ratio > 1).sum()), worst, float(err.max()), float(np.abs(ref).max()))
+    return worst

@@ -35,6 +35,7 @@ def test_header_declares_the_boundary():
     for name in ("fattn_fwd", "fattn_fwd_gqa", "fattn_fwd_host", "fattn_plan",
                  "fattn_get_device_status", "fattn_selftest_wait_timeout",
                  "fattn_fwd_unfused", "fattn_unfused_workspace_bytes",
+                 "fattn_bwd", "fattn_bwd_workspace_bytes",
                  "fattn_status_string", "fattn_version"):
         assert name in syms
 
@@ -109,6 +110,32 @@ def test_unfused_workspace_bytes(lib):
         assert lib.fattn_unfused_workspace_bytes(B, H, N) == 0
 
 
+def test_bwd_workspace_and_argument_errors(lib):
+    for (B, H, N) in ((1, 1, 1), (2, 3, 129), (4, 16, 4096), (1, 16, 16000)):
+        assert lib.fattn_bwd_workspace_bytes(B, H, N) == 8 * B * H * (-(-N // 128) * 128)
+    assert lib.fattn_bwd_workspace_bytes(0, 1, 1) == 0
+    T = 1 << 40  # far-apart fake device addresses, never dereferenced
+
+    def bwd(q=T, k=2 * T, v=3 * T, o=4 * T, do=5 * T, lse=6 * T, dq=7 * T, dk=8 * T, dv=9 * T,
+            ws=10 * T, wsb=None, B=1, H=2, N=16, D=64, dtype=2):
+        if wsb is None:
+            wsb = lib.fattn_bwd_workspace_bytes(B, H, N)
+        return lib.fattn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, wsb, B, H, N, D, 0.125, 1,
+                             dtype, None)
+    assert bwd(dtype=0) == UNSUPPORTED
+    assert bwd(D=96) == UNSUPPORTED
+    assert bwd(do=None) == INVALID
+    assert bwd(lse=None) == INVALID
+    assert bwd(ws=None) == INVALID
+    assert bwd(wsb=100) == INVALID
+    assert bwd(dk=8 * T + 8) == MISALIGNED
+    assert bwd(lse=6 * T + 2) == MISALIGNED
+    assert bwd(dk=7 * T) == INVALID          # dK over dQ
+    assert bwd(dv=4 * T) == INVALID          # dV over O
+    assert bwd(ws=2 * T) == INVALID          # workspace over K
+    assert bwd(B=0) == OK
+
+
 def test_unfused_argument_errors(lib):
     WS = FAKE + (8 << 20)
 
@@ -140,6 +167,9 @@ def test_empty_problem_is_ok_and_enqueues_nothing(lib):
 def test_valid_call_without_a_device_reports_no_device(lib):
     assert call_fwd(lib) == NO_DEVICE
     assert call_fwd(lib, dtype=0) == NO_DEVICE
+    T = 1 << 40
+    assert lib.fattn_bwd(T, 2 * T, 3 * T, 4 * T, 5 * T, 6 * T, 7 * T, 8 * T, 9 * T, 10 * T, 1 << 20,
+                         1, 1, 16, 64, 0.125, 0, 2, None) == NO_DEVICE
     ws = FAKE + (8 << 20)
     assert lib.fattn_fwd_unfused(FAKE, FAKE + (1 << 16), FAKE + (2 << 16), FAKE + (3 << 16), None,
                                  ws, 1 << 20, 1, 1, 16, 64, 0.125, 1, 2, None) == NO_DEVICE

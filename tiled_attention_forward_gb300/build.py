@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfattn.so")
-SOURCES = ["fattn_api.cu", "fwd_tc.cu", "fwd_ffma.cu", "fwd_unfused.cu"]
+SOURCES = ["fattn_api.cu", "fwd_tc.cu", "fwd_ffma.cu", "fwd_unfused.cu", "bwd_tc.cu"]
 HEADERS = ["internal.h", "sm103_ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

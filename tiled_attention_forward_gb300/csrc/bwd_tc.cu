@@ -1,0 +1,482 @@
+// bwd_tc.cu -- attention backward (dQ, dK, dV) on the tensor cores, bf16/fp16.
+//
+// The FA2 report of chang-wenbin.github.io (section "反向传播性能分析") keeps
+// the forward's tiling for the backward pass and recomputes the scores
+// instead of storing them.  Per (query i, key j) pair, with P_ij rebuilt from
+// the LSE the forward emitted:
+//   P_ij = exp(s_ij - LSE_i),  dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - Delta_i)
+//   dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j
+// where Delta_i = dO_i . O_i.
+//
+// Three kernels:
+//   prep : per row, Delta_i and LSE_i * log2(e) into a padded workspace
+//          (+inf / 0 past N so that tail rows contribute nothing);
+//   dKdV : one CTA per (head, 128-key block): K and V stay in shared memory
+//          while the 128-query tiles of Q, dO and their row statistics stream
+//          through a TMA ring; S^T = K Q^T and dP^T = V dO^T land in TMEM,
+//          four warps (one key row per thread) turn them into P^T and dS^T
+//          (16-bit, written back into TMEM), and dV += P^T dO, dK += dS^T Q
+//          accumulate in TMEM; dK and dV are written once at the end;
+//   dQ   : one CTA per (head, 128-query tile), the mirror image: Q and dO
+//          stay, K and V stream, S = Q K^T and dP = dO V^T, dS formed per
+//          query row, dQ += dS K accumulates in TMEM.
+// The page has the K/V gradients updated in place with atomics; here each
+// gradient is owned by exactly one CTA (no atomics, a deterministic result),
+// at the price of recomputing S and dP once more for dQ (7 products of
+// 128 x 128 x D per tile pair instead of 5).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fattn {
+namespace {
+
+// Error word of this translation unit's kernels (ORed into the status call).
+__device__ uint32_t g_error_word;
+
+constexpr int kBT = 128;            // tile edge: rows of every tile, keys / queries per tile
+constexpr int kBwdThreads = 192;    // warps 0-3 elementwise, warp 4 MMA, warp 5 TMA
+constexpr uint32_t kTmemCols = 512;
+
+template <int D, bool KV>
+struct BwdLayout {
+    static constexpr int kTile = kBT * D * 2;               // one [128][D] 16-bit tile
+    static constexpr int kStats = KV ? 2 * kBT * 4 : 0;     // LSE*log2e and Delta of 128 queries
+    static constexpr int kStages = D == 128 ? 2 : 4;
+    static constexpr int kStageBytes = (2 * kTile + kStats + 1023) / 1024 * 1024;
+    static constexpr int kOuter = 0;                        // two resident tiles
+    static constexpr int kRing = 2 * kTile;
+    static constexpr int kBar = kRing + kStages * kStageBytes;
+    // barriers: outer_full, full[S], empty[S], s_full, p_full, done; abort flag; TMEM slot
+    static constexpr int kBytes = kBar + (4 + 2 * kStages) * 8 + 16;
+    static_assert(kBytes <= 227 * 1024, "shared memory");
+};
+
+struct BwdBars {
+    uint64_t* outer_full;
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* s_full;
+    uint64_t* p_full;
+    uint64_t* done;
+    uint32_t* abort_flag;
+    uint32_t* tmem_slot;
+};
+
+template <int D, bool KV>
+__device__ __forceinline__ BwdBars bwd_bars(uint8_t* smem) {
+    using L = BwdLayout<D, KV>;
+    BwdBars b;
+    uint64_t* p = reinterpret_cast<uint64_t*>(smem + L::kBar);
+    b.outer_full = p;
+    b.full = p + 1;
+    b.empty = b.full + L::kStages;
+    b.s_full = b.empty + L::kStages;
+    b.p_full = b.s_full + 1;
+    b.done = b.p_full + 1;
+    b.abort_flag = reinterpret_cast<uint32_t*>(b.done + 1);
+    b.tmem_slot = b.abort_flag + 1;
+    return b;
+}
+
+__device__ __forceinline__ uint32_t pack16(float lo, float hi, bool bf16) {
+    if (bf16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// One-dimensional bulk copy global -> shared, completion as tx bytes on `bar`
+// (both addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t* abort_flag,
+                                          uint64_t timeout_ns) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort_flag, &g_error_word,
+                                                     timeout_ns));
+}
+
+// Work unit of a CTA.  dKdV: key block kb of head bh, query tiles j0 .. nt-1
+// (causal: from the diagonal tile on; ascending kb = longest first).  dQ:
+// query tile qt of head bh, key tiles 0 .. j_end-1 (causal: up to the
+// diagonal; descending qt = longest first).
+struct BwdTask {
+    int bh, blk, j0, n;
+};
+
+template <bool KV, bool CAUSAL>
+__device__ __forceinline__ BwdTask bwd_task(const BwdArgs& a) {
+    BwdTask t;
+    const int idx = blockIdx.x;
+    t.bh = idx % a.BH;
+    if (KV) {
+        t.blk = idx / a.BH;
+        t.j0 = CAUSAL ? t.blk : 0;
+        t.n = a.num_tiles - t.j0;
+    } else {
+        t.blk = CAUSAL ? a.num_tiles - 1 - idx / a.BH : idx / a.BH;
+        t.j0 = 0;
+        t.n = CAUSAL ? t.blk + 1 : a.num_tiles;
+    }
+    return t;
+}
+
+template <int D, bool BF16, bool KV, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdArgs a) {
+    using L = BwdLayout<D, KV>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if ((smem_u32(smem) & 1023u) != 0u) {
+        if (threadIdx.x == 0) atomicOr(&g_error_word, 1u << kDevErrInternal);
+        return;
+    }
+    const BwdBars bars = bwd_bars<D, KV>(smem);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const BwdTask tk = bwd_task<KV, CAUSAL>(a);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bars.outer_full, 1);
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(&bars.full[s], 1);
+            mbar_init(&bars.empty[s], 1);
+        }
+        mbar_init(bars.s_full, 1);
+        mbar_init(bars.p_full, 4);
+        mbar_init(bars.done, 1);
+        *bars.abort_flag = 0u;
+        fence_barrier_init();
+    }
+    if (warp == 4) {
+        tmem_alloc(bars.tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *bars.tmem_slot;
+    // TMEM columns: S (or S^T) [0,128), dP [128,256), acc1 [256,256+D), acc2 [256+D,256+2D).
+    // The 16-bit P and dS overwrite the first 64 columns of S and dP.
+    const uint32_t t_s = tmem, t_dp = tmem + 128, t_acc1 = tmem + 256, t_acc2 = tmem + 256 + D;
+    const int blk0 = tk.blk * kBT;  // first row of the resident tiles
+    const int kvh = tk.bh;          // multi-head: K/V head = query head
+
+    if (warp == 5) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            const CUtensorMap* outer1 = KV ? &a.tmap_k : &a.tmap_q;
+            const CUtensorMap* outer2 = KV ? &a.tmap_v : &a.tmap_do;
+            const CUtensorMap* inner1 = KV ? &a.tmap_q : &a.tmap_k;
+            const CUtensorMap* inner2 = KV ? &a.tmap_do : &a.tmap_v;
+            mbar_arrive_expect_tx(bars.outer_full, 2 * L::kTile);
+            for (int at = 0; at < D / 64; ++at) {
+                tma_load_3d(smem + L::kOuter + at * kBT * 128, outer1, bars.outer_full, at * 64, blk0, kvh);
+                tma_load_3d(smem + L::kOuter + L::kTile + at * kBT * 128, outer2, bars.outer_full, at * 64,
+                            blk0, kvh);
+            }
+            int issued = 0;
+            bool ok = true;
+            for (int it = 0; it < tk.n && ok; ++it) {
+                const int s = it % L::kStages;
+                if (it >= L::kStages) {
+                    ok = mbar_wait_bounded(&bars.empty[s], ((it / L::kStages) - 1) & 1u, bars.abort_flag,
+                                           &g_error_word, a.timeout_ns);
+                    if (!ok) break;
+                }
+                const int row0 = (tk.j0 + it) * kBT;
+                uint8_t* st = smem + L::kRing + s * L::kStageBytes;
+                mbar_arrive_expect_tx(&bars.full[s], 2 * L::kTile + L::kStats);
+                for (int at = 0; at < D / 64; ++at) {
+                    tma_load_3d(st + at * kBT * 128, inner1, &bars.full[s], at * 64, row0, kvh);
+                    tma_load_3d(st + L::kTile + at * kBT * 128, inner2, &bars.full[s], at * 64, row0, kvh);
+                }
+                if (KV) {
+                    const float* stats = a.ws + static_cast<int64_t>(tk.bh) * 2 * a.Npad + row0;
+                    bulk_load(st + 2 * L::kTile, stats, kBT * 4, &bars.full[s]);
+                    bulk_load(st + 2 * L::kTile + kBT * 4, stats + a.Npad, kBT * 4, &bars.full[s]);
+                }
+                ++issued;
+            }
+            if (!ok) {
+                // Let the copies already started land before the CTA leaves.
+                for (int s = 0; s < L::kStages; ++s) {
+                    int last = -1;
+                    for (int i = 0; i < issued; ++i)
+                        if (i % L::kStages == s) last = i;
+                    if (last >= 0)
+                        mbar_wait_bounded(&bars.full[s], (last / L::kStages) & 1u, nullptr, &g_error_word,
+                                          a.timeout_ns);
+                }
+                mbar_wait_bounded(bars.outer_full, 0u, nullptr, &g_error_word, a.timeout_ns);
+            }
+        }
+    } else if (warp == 4) {
+        // ---------------- MMA issue (one elected lane) ----------------
+        constexpr uint32_t kIdescS = idesc_f16_f32(kBT, kBT, BF16 ? 1u : 0u, 0u, 0u);
+        constexpr uint32_t kIdescAcc = idesc_f16_f32(kBT, D, BF16 ? 1u : 0u, 0u, 1u);
+        const uint64_t kmaj = smem_desc_sw128(0u, 16u, 1024u);
+        const uint64_t mnmaj = smem_desc_sw128(0u, kBT * 128u, 1024u);
+        const uint32_t outer1_s = smem_u32(smem + L::kOuter), outer2_s = outer1_s + L::kTile;
+        bool ok = warp_wait(bars.outer_full, 0u, bars.abort_flag, a.timeout_ns);
+        for (int it = 0; it < tk.n && ok; ++it) {
+            const int s = it % L::kStages;
+            ok = warp_wait(&bars.full[s], (it / L::kStages) & 1u, bars.abort_flag, a.timeout_ns);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t inner1_s = smem_u32(smem + L::kRing + s * L::kStageBytes);
+            const uint32_t inner2_s = inner1_s + L::kTile;
+            if (elect_one_sync()) {
+                // S = outer1 inner1^T and dP = outer2 inner2^T: both operands K-major over D.
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = ((kk / 4) * (kBT * 128) + (kk % 4) * 32) >> 4;
+                    mma_ss(t_s, kmaj + (outer1_s >> 4) + off, kmaj + (inner1_s >> 4) + off, kIdescS,
+                           kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = ((kk / 4) * (kBT * 128) + (kk % 4) * 32) >> 4;
+                    mma_ss(t_dp, kmaj + (outer2_s >> 4) + off, kmaj + (inner2_s >> 4) + off, kIdescS,
+                           kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bars.s_full);
+            }
+            __syncwarp();
+            ok = warp_wait(bars.p_full, it & 1u, bars.abort_flag, a.timeout_ns);
+            if (!ok) break;
+            tc_fence_after();
+            if (elect_one_sync()) {
+                // acc (+)= (16-bit tile in TMEM, 8 columns per 16 rows of the
+                // inner tile) x inner tile as an MN-major operand.
+#pragma unroll
+                for (int kk = 0; kk < kBT / 16; ++kk) {
+                    const uint64_t boff = (kk * 16 * 128) >> 4;
+                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                    if (KV) {
+                        mma_ts(t_acc1, t_s + kk * 8, mnmaj + (inner2_s >> 4) + boff, kIdescAcc, acc);   // dV += P^T dO
+                        mma_ts(t_acc2, t_dp + kk * 8, mnmaj + (inner1_s >> 4) + boff, kIdescAcc, acc);  // dK += dS^T Q
+                    } else {
+                        mma_ts(t_acc1, t_dp + kk * 8, mnmaj + (inner1_s >> 4) + boff, kIdescAcc, acc);  // dQ += dS K
+                    }
+                }
+                mma_commit(&bars.empty[s]);
+            }
+            __syncwarp();
+        }
+        if (elect_one_sync()) mma_commit(bars.done);  // fires once every MMA above has completed
+        __syncwarp();
+    } else {
+        // ---------------- elementwise warps 0-3: thread = TMEM lane = resident row ----------------
+        const int r = warp * 32 + lane;
+        const int row = blk0 + r;  // KV: key index; dQ: query index
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        float lse2_r = 0.f, delta_r = 0.f;
+        if (!KV) {
+            const float* stats = a.ws + static_cast<int64_t>(tk.bh) * 2 * a.Npad + row;
+            lse2_r = stats[0];        // +inf past N: the row's P is 0
+            delta_r = stats[a.Npad];
+        }
+        bool ok = true;
+        for (int it = 0; it < tk.n && ok; ++it) {
+            const int j = tk.j0 + it;
+            const int s = it % L::kStages;
+            ok = warp_wait(bars.s_full, it & 1u, bars.abort_flag, a.timeout_ns);
+            if (KV && ok)  // the stage's statistics: this phase is complete and not yet refilled
+                ok = warp_wait(&bars.full[s], (it / L::kStages) & 1u, bars.abort_flag, a.timeout_ns);
+            if (!ok) break;
+            tc_fence_after();
+            const float* lse2s = reinterpret_cast<const float*>(smem + L::kRing + s * L::kStageBytes + 2 * L::kTile);
+            const float* deltas = lse2s + kBT;
+            const bool diag = CAUSAL && j == tk.blk;
+#pragma unroll 1
+            for (int c = 0; c < kBT / 32; ++c) {
+                uint32_t sv[32], dpv[32];
+                tmem_ld32(t_s + lane_off + c * 32, sv);
+                tmem_ld32(t_dp + lane_off + c * 32, dpv);
+                tmem_wait_ld();
+                reg_fence(sv);
+                reg_fence(dpv);
+                uint32_t pk[16], dsk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float p[2], ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int col = c * 32 + e + u;  // KV: query j*128+col; dQ: key j*128+col
+                        const float lse2 = KV ? lse2s[col] : lse2_r;
+                        const float dlt = KV ? deltas[col] : delta_r;
+                        float pv = ex2_approx(__uint_as_float(sv[e + u]) * a.sl2 - lse2);
+                        if (KV) {
+                            if (diag && col < r) pv = 0.f;  // query j*128+col before key row
+                        } else {
+                            const int key = j * kBT + col;
+                            if (key >= a.N || (diag && col > r)) pv = 0.f;
+                        }
+                        p[u] = pv;
+                        ds[u] = pv * (__uint_as_float(dpv[e + u]) - dlt);
+                    }
+                    pk[e / 2] = pack16(p[0], p[1], BF16);
+                    dsk[e / 2] = pack16(ds[0], ds[1], BF16);
+                }
+                if (KV) tmem_st16(t_s + lane_off + c * 16, pk);
+                tmem_st16(t_dp + lane_off + c * 16, dsk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.p_full);
+        }
+        // ---------------- epilogue: accumulators -> 16-bit rows ----------------
+        const bool fin = warp_wait(bars.done, 0u, nullptr, a.timeout_ns);
+        tc_fence_after();
+        const int64_t out_row = static_cast<int64_t>(tk.bh) * a.N + row;
+#pragma unroll 1
+        for (int acc = 0; acc < (KV ? 2 : 1); ++acc) {
+            // KV: acc 0 = dV (no scale), acc 1 = dK (x scale); dQ: acc 0 = dQ (x scale)
+            const uint32_t tacc = (acc == 0 ? t_acc1 : t_acc2) + lane_off;
+            const float mul = (KV && acc == 0) ? 1.f : a.scale;
+            void* base = KV ? (acc == 0 ? a.dv : a.dk) : a.dq;
+            uint8_t* orow = reinterpret_cast<uint8_t*>(base) + out_row * D * 2;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tacc + c * 32, v);  // warp-collective: every lane, whatever its row
+                tmem_wait_ld();
+                reg_fence(v);
+                if (fin && row < a.N) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul, BF16);
+                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Delta_i = dO_i . O_i (fp32 over the 16-bit inputs) and LSE_i * log2(e),
+// one warp per row of the padded workspace [B*H][2][Npad]; rows past N get
+// +inf and 0.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const void* __restrict__ o,
+                                                            const void* __restrict__ dout,
+                                                            const float* __restrict__ lse,
+                                                            float* __restrict__ ws, int N, int Npad,
+                                                            int64_t rows_padded) {
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+    const int lane = threadIdx.x % 32;
+    if (gw >= rows_padded) return;
+    const int64_t bh = gw / Npad;
+    const int i = static_cast<int>(gw % Npad);
+    float lse2 = INFINITY, delta = 0.f;
+    if (i < N) {
+        const int64_t row = bh * N + i;
+        constexpr int kPer = D / 32;  // 16-bit elements per lane: 2 or 4
+        const uint16_t* orow = reinterpret_cast<const uint16_t*>(o) + row * D + lane * kPer;
+        const uint16_t* drow = reinterpret_cast<const uint16_t*>(dout) + row * D + lane * kPer;
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+            float x, y;
+            if (BF16) {
+                x = __bfloat162float(__ushort_as_bfloat16(orow[e]));
+                y = __bfloat162float(__ushort_as_bfloat16(drow[e]));
+            } else {
+                x = __half2float(__ushort_as_half(orow[e]));
+                y = __half2float(__ushort_as_half(drow[e]));
+            }
+            acc = fmaf(x, y, acc);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        delta = acc;
+        lse2 = lse[row] * 1.4426950408889634f;
+    }
+    if (lane == 0) {
+        ws[bh * 2 * Npad + i] = lse2;
+        ws[(bh * 2 + 1) * Npad + i] = delta;
+    }
+}
+
+template <typename K>
+cudaError_t opt_in_smem(K* fn, int bytes, bool (&done)[kMaxDevices]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices || !done[dev]) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t bwd_launch_all(const BwdArgs& a, const void* o, const void* dout, const float* lse,
+                           cudaStream_t stream) {
+    const int64_t rows_padded = static_cast<int64_t>(a.BH) * a.Npad;
+    attn_bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((rows_padded + 7) / 8), 256, 0, stream>>>(
+        o, dout, lse, a.ws, a.N, a.Npad, rows_padded);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(a.num_tiles) * a.BH);
+    static bool kv_done[kMaxDevices] = {};
+    static bool q_done[kMaxDevices] = {};
+    auto* kkv = attn_bwd_kernel<D, BF16, true, CAUSAL>;
+    if ((e = opt_in_smem(kkv, BwdLayout<D, true>::kBytes, kv_done)) != cudaSuccess) return e;
+    kkv<<<grid, kBwdThreads, BwdLayout<D, true>::kBytes, stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    auto* kq = attn_bwd_kernel<D, BF16, false, CAUSAL>;
+    if ((e = opt_in_smem(kq, BwdLayout<D, false>::kBytes, q_done)) != cudaSuccess) return e;
+    kq<<<grid, kBwdThreads, BwdLayout<D, false>::kBytes, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t bwd_padded_rows(int64_t N) { return (N + kBT - 1) / kBT * kBT; }
+
+cudaError_t bwd_launch(const BwdArgs& a, const void* o, const void* dout, const float* lse, int D,
+                       bool bf16, bool causal, cudaStream_t s) {
+    if (D == 128) {
+        if (bf16) return causal ? bwd_launch_all<128, true, true>(a, o, dout, lse, s)
+                                : bwd_launch_all<128, true, false>(a, o, dout, lse, s);
+        return causal ? bwd_launch_all<128, false, true>(a, o, dout, lse, s)
+                      : bwd_launch_all<128, false, false>(a, o, dout, lse, s);
+    }
+    if (bf16) return causal ? bwd_launch_all<64, true, true>(a, o, dout, lse, s)
+                            : bwd_launch_all<64, true, false>(a, o, dout, lse, s);
+    return causal ? bwd_launch_all<64, false, true>(a, o, dout, lse, s)
+                  : bwd_launch_all<64, false, false>(a, o, dout, lse, s);
+}
+
+cudaError_t bwd_read_and_clear_error_word(uint32_t* out) {
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v));
+    if (e != cudaSuccess) return e;
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+    *out = v;
+    return e;
+}
+
+}  // namespace fattn

@@ -368,14 +368,83 @@ int fattn_fwd_unfused_static(const void* q, const void* k, const void* v, void* 
                              N, D, scale, causal, dtype, stream_h);
 }
 
+int64_t fattn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N) {
+    if (B <= 0 || H <= 0 || N <= 0) return 0;
+    if (B > (int64_t(1) << 30) || H > (int64_t(1) << 30) || N > (int64_t(1) << 30) ||
+        B * H > (int64_t(1) << 30))
+        return 0;
+    return B * H * 2 * bwd_padded_rows(N) * static_cast<int64_t>(sizeof(float));
+}
+
+int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+              const float* lse, void* dq, void* dk, void* dv, void* workspace,
+              int64_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t D, float scale,
+              int causal, int dtype, fattn_stream_t stream_h) {
+    bool empty = false;
+    // q, k, v and dq share the forward's rules (dq plays O's part).
+    int st = validate(q, k, v, dq, nullptr, B, H, H, N, D, scale, dtype, &empty);
+    if (st != FATTN_OK || empty) return st;
+    if (dtype == FATTN_F32) return FATTN_ERR_UNSUPPORTED;
+    if (!o || !dout || !lse || !dk || !dv || !workspace) return FATTN_ERR_INVALID_ARG;
+    if (!aligned16(o) || !aligned16(dout) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return FATTN_ERR_MISALIGNED;
+    const int64_t BH = B * H;
+    const int64_t need = fattn_bwd_workspace_bytes(B, H, N);
+    if (need <= 0) return FATTN_ERR_UNSUPPORTED;
+    if (bwd_padded_rows(N) / 128 * BH > 0x7fffffffll) return FATTN_ERR_UNSUPPORTED;
+    if (workspace_bytes < need) return FATTN_ERR_INVALID_ARG;
+    const size_t bytes = static_cast<size_t>(BH * N * D) * 2u;
+    const size_t lb = static_cast<size_t>(BH * N) * sizeof(float);
+    const void* ins[6] = {q, k, v, o, dout, lse};
+    const size_t in_sz[6] = {bytes, bytes, bytes, bytes, bytes, lb};
+    void* outs[4] = {dq, dk, dv, workspace};
+    const size_t out_sz[4] = {bytes, bytes, bytes, static_cast<size_t>(need)};
+    for (int i = 0; i < 4; ++i) {
+        for (int j = 0; j < 6; ++j)
+            if (overlaps(outs[i], out_sz[i], ins[j], in_sz[j])) return FATTN_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 4; ++j)
+            if (overlaps(outs[i], out_sz[i], outs[j], out_sz[j])) return FATTN_ERR_INVALID_ARG;
+    }
+    int sms = 0;
+    st = current_sm_count(&sms);
+    if (st != FATTN_OK) return st;
+    const bool bf16 = dtype == FATTN_BF16;
+    BwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    TcArgs t;
+    std::memset(&t, 0, sizeof(t));
+    if (tc_encode_maps(t, q, k, v, BH, BH, N, D, bf16) != cudaSuccess) return FATTN_ERR_CUDA;
+    a.tmap_q = t.tmap_q;
+    a.tmap_k = t.tmap_k;
+    a.tmap_v = t.tmap_v;
+    if (tc_encode_maps(t, dout, dout, dout, BH, BH, N, D, bf16) != cudaSuccess) return FATTN_ERR_CUDA;
+    a.tmap_do = t.tmap_q;
+    a.ws = static_cast<float*>(workspace);
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.N = static_cast<int>(N);
+    a.Npad = static_cast<int>(bwd_padded_rows(N));
+    a.BH = static_cast<int>(BH);
+    a.num_tiles = a.Npad / 128;
+    a.sl2 = scale * kLog2e;
+    a.scale = scale;
+    a.timeout_ns = kDefaultTimeoutNs;
+    cudaError_t e = bwd_launch(a, o, dout, lse, static_cast<int>(D), bf16, causal != 0,
+                               reinterpret_cast<cudaStream_t>(stream_h));
+    return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
 int fattn_get_device_status(fattn_stream_t stream_h) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FATTN_ERR_CUDA;
-    uint32_t word = 0, word_unfused = 0;
+    uint32_t word = 0, word_unfused = 0, word_bwd = 0;
     if (read_and_clear_error_word(&word) != cudaSuccess ||
-        unfused_read_and_clear_error_word(&word_unfused) != cudaSuccess)
+        unfused_read_and_clear_error_word(&word_unfused) != cudaSuccess ||
+        bwd_read_and_clear_error_word(&word_bwd) != cudaSuccess)
         return FATTN_ERR_CUDA;
-    word |= word_unfused;
+    word |= word_unfused | word_bwd;
     if (word & (1u << FATTN_ERR_INTERNAL)) return FATTN_ERR_INTERNAL;
     if (word & (1u << FATTN_ERR_TIMEOUT)) return FATTN_ERR_TIMEOUT;
     return FATTN_OK;

@@ -77,6 +77,30 @@ cudaError_t unfused_read_and_clear_error_word(uint32_t* out);
 constexpr size_t kUnfusedStaticBytes = size_t(64) << 20;
 cudaError_t unfused_static_scratch(void** ptr);
 
+// ---- backward (bf16 / fp16), bwd_tc.cu --------------------------------------
+struct BwdArgs {
+    CUtensorMap tmap_q;   // 3-D {D, N, B*H}, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tmap_k;
+    CUtensorMap tmap_v;
+    CUtensorMap tmap_do;
+    float* ws;            // [B*H][2][Npad]: LSE*log2(e) (+inf past N), Delta (0 past N)
+    void* dq;             // [B,H,N,D] outputs, input dtype
+    void* dk;
+    void* dv;
+    int N;
+    int Npad;             // N rounded up to 128
+    int BH;
+    int num_tiles;        // Npad / 128
+    float sl2;            // scale * log2(e)
+    float scale;
+    uint64_t timeout_ns;
+};
+
+int64_t bwd_padded_rows(int64_t N);
+cudaError_t bwd_launch(const BwdArgs& a, const void* o, const void* dout, const float* lse, int D,
+                       bool bf16, bool causal, cudaStream_t s);
+cudaError_t bwd_read_and_clear_error_word(uint32_t* out);
+
 // Key/value head read by query head bh = b*H + h: b*Hkv + h / (H/Hkv).
 __host__ __device__ __forceinline__ int kv_head_of(int bh, int H, int Hkv) {
     return (bh / H) * Hkv + (bh % H) / (H / Hkv);
