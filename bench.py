@@ -1,7 +1,7 @@
 """Benchmark of the attention forward on GB300 (one JSON line on stdout).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference|unfused]
+                    [--impl ours|reference|unfused] [--pass fwd|bwd]
 
 A step is one attention forward (the whole hot path: one kernel launch) over
 the named workload's synthetic seeded inputs, already resident in HBM.
@@ -22,6 +22,12 @@ pinned memory, the kernel and the device->host copy of O and LSE.
 `cpu_baseline` is the fp64 CPU oracle as it stands, timed on this host's cores
 on a bounded sample of the same workload (a set of random query rows).
 `--impl reference` times that oracle alone (the reference arm of this method).
+
+`--pass bwd` times the backward pass instead (fattn_bwd: dQ, dK, dV from
+Q, K, V, O, LSE and a seeded dO, three kernels per step) under the same
+rules; its FLOP count is 2.5x the forward's (five products of the size of
+the forward's two), and its cpu_baseline / reference arm is the oracle's
+backward on whole heads of the workload.
 
 `--impl unfused` times the library's materialising comparator
 (fattn_fwd_unfused: S and P written to HBM, three kernels per step) on the
@@ -48,6 +54,8 @@ if ROOT not in sys.path:
 from tiled_attention_forward_gb300.inputs import BY_NAME, HEADLINE, workload_inputs  # noqa: E402
 
 METRIC = "attn fwd TFLOP/s (B=4,H=16,N=4096,D=128 bf16) and % of GB300 BF16 peak"
+METRIC_BWD = "attn bwd TFLOP/s (5-product convention, 2.5x fwd FLOP) and % of GB300 BF16 peak"
+BWD_FLOP_FACTOR = 2.5
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the kernel on each workload, from an ncu capture (summaries under profiles/),
@@ -377,6 +385,192 @@ def run_ours(args, w, ws, rank, local):
     return line
 
 
+def oracle_bwd_rate(w, q, k, v, do, target_s):
+    """Times the oracle's backward on whole heads of the workload (as many as
+    fit in about target_s seconds); returns (FLOP in the backward convention,
+    seconds, heads, threads)."""
+    import oracle
+    heads_total = w.B * w.H
+    qh, kh, vh, dh = (t.reshape(1, heads_total, w.N, w.D) for t in (q, k, v, do))
+    done, secs, n = 0, 0.0, 1
+    while done < heads_total:
+        n = min(n, heads_total - done)
+        sl = slice(done, done + n)
+        args = [t[:, sl].to(torch.float64).numpy() for t in (qh, kh, vh, dh)]
+        t0 = time.perf_counter()
+        oracle.backward(*args, w.scale, w.causal)
+        dt = time.perf_counter() - t0
+        secs += dt
+        done += n
+        if secs >= target_s:
+            break
+        n = max(1, min(2 * n, int(n * (target_s - secs) / max(dt, 1e-3))))
+    per_head = w.flops() / heads_total
+    return BWD_FLOP_FACTOR * per_head * done, secs, done, oracle.default_threads()
+
+
+def bwd_inputs(w):
+    q, k, v = workload_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 50)
+    do = torch.randn(q.shape, generator=g).to(q.dtype)
+    return q, k, v, do
+
+
+def run_ours_bwd(args, w, ws, rank, local):
+    """The backward pass: one step = fattn_bwd over the workload (statistics,
+    dK/dV and dQ kernels), inputs (Q, K, V, O, LSE, dO) resident in HBM."""
+    import tiled_attention_forward_gb300 as fattn
+
+    if w.dtype == "fp32":
+        raise SystemExit("--pass bwd covers bf16 / fp16 workloads only")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    q, k, v, do = bwd_inputs(w)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fattn.fwd(qd, kd, vd, causal=w.causal, scale=w.scale)
+    dq, dk, dv = (torch.empty_like(qd) for _ in range(3))
+    wsp = torch.empty(fattn.bwd_workspace_bytes(w.B, w.H, w.N), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fattn.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv,
+                  workspace=wsp, stream=stream)
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fattn.get_device_status(stream) != 0:
+        raise RuntimeError("device status after warm-up")
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t1 = time.time()
+    time.sleep(0.15)
+    sampler.stop()
+    status = fattn.get_device_status(stream)
+    if status != 0:
+        raise RuntimeError("device status %s during the timed region" % fattn.status_string(status))
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_total = float(sum(per))
+
+    # end to end through the public API: pinned host inputs copied in, the
+    # backward, the three gradients copied back, every step
+    e2e_ms, h2d, d2h = float("nan"), 0, 0
+    if not args.no_e2e:
+        hosts = [t.pin_memory() for t in (q, k, v, do)] + [o.cpu().pin_memory(), lse.cpu().pin_memory()]
+        devs = [qd, kd, vd, dod, o, lse]
+        outs_h = [torch.empty_like(q).pin_memory() for _ in range(3)]
+        n_e2e = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            for hsrc, ddst in zip(hosts, devs):
+                ddst.copy_(hsrc, non_blocking=True)
+            step()
+            for hdst, dsrc in zip(outs_h, (dq, dk, dv)):
+                hdst.copy_(dsrc, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        es.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        ee.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = es.elapsed_time(ee) / n_e2e
+        h2d = sum(t.numel() * t.element_size() for t in hosts)
+        d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], device=dev)
+    clocks = sampler.summary(t0, t1)
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return None
+    flops = BWD_FLOP_FACTOR * w.flops()
+    ms_per_step = ms_total / args.steps
+    value = whole_job_tflops(flops, ws, args.steps, ms_total)
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+            "traffic": None, "scope": "the whole three-kernel step (statistics, dK/dV, dQ)",
+            "peak_source": "bf16_tflops dense bf16 (cuBLAS burst) of %s; fp16 taken at the same rate" % peak_src,
+            "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+            "executed_tensor_tflops": achieved * 7.0 / 5.0,
+            "note": "algorithmic FLOP = 5 products of 128x128xD per tile pair; the kernels execute 7 "
+                    "(S and dP are formed once for dK/dV and once for dQ)"}
+    line = {
+        "metric": METRIC_BWD, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_median": statistics.median(per),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": DTYPE_NAMES[w.dtype], "data": "synthetic (seeded iid normal Q, K, V, dO)",
+        "config": dict(config_of(w, ws), **{"pass": "bwd"}), "pct_of_peak": 100.0 * roof["frac"],
+        "roofline": roof,
+        "e2e": ({"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                 "api": "torch pinned-host copies + tiled_attention_forward_gb300.bwd"}
+                if not args.no_e2e else None),
+        "gpu_launches": 3 * args.steps, "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        fl, secs, heads, threads = oracle_bwd_rate(w, q, k, v, do, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": fl / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": "fp64 C oracle backward on %d whole head(s) of the workload "
+                                          "(%.1f s)" % (heads, secs)}
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return line
+
+
+def run_reference_bwd(args, w, ws, rank):
+    if rank != 0:
+        return None
+    q, k, v, do = bwd_inputs(w)
+    per_step_s = max(0.5, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_bwd_rate(w, q, k, v, do, min(per_step_s, 1.0))
+    fl_tot, secs_tot, heads_tot, threads = 0.0, 0.0, 0, 1
+    for _ in range(args.steps):
+        fl, s, h, threads = oracle_bwd_rate(w, q, k, v, do, per_step_s)
+        fl_tot += fl
+        secs_tot += s
+        heads_tot += h
+    value = fl_tot / secs_tot / 1e12 if secs_tot > 0 else 0.0
+    sample = "%d whole heads over %d steps (%.1f s), fp64 C oracle backward" % (heads_tot, args.steps, secs_tot)
+    return {
+        "impl": "reference", "metric": METRIC_BWD, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs_tot / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded iid normal Q, K, V, dO)",
+        "config": dict(config_of(w, 1), **{"pass": "bwd"}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
 def run_e2e(fattn, w, q, k, v, qd, kd, vd, o, lse, stream, dev, steps, barrier):
     """Per step: H2D of Q, K, V from pinned memory, the kernel, D2H of O and LSE,
     all enqueued by the library's host-buffer entry point."""
@@ -436,6 +630,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference", "unfused"])
+    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall time of the CPU oracle sample (cpu_baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -445,7 +640,12 @@ def main():
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_env()
     w = BY_NAME[args.workload]
-    if args.impl == "reference":
+    if args.pass_ == "bwd":
+        if args.impl == "unfused":
+            ap.error("--impl unfused is a forward comparator")
+        line = run_reference_bwd(args, w, ws, rank) if args.impl == "reference" else \
+            run_ours_bwd(args, w, ws, rank, local)
+    elif args.impl == "reference":
         line = run_reference(args, w, ws, rank)
     else:
         line = run_ours(args, w, ws, rank, local)
