@@ -14,7 +14,8 @@
 //   dKdV : one CTA per (head, 128-key block): K and V stay in shared memory
 //          while the 128-query tiles of Q, dO and their row statistics stream
 //          through a TMA ring; S^T = K Q^T and dP^T = V dO^T land in TMEM,
-//          four warps (one key row per thread) turn them into P^T and dS^T
+//          eight warps (one key row per thread, two warps per row range,
+//          64 columns each) turn them into P^T and dS^T
 //          (16-bit, written back into TMEM), and dV += P^T dO, dK += dS^T Q
 //          accumulate in TMEM; dK and dV are written once at the end;
 //   dQ   : one CTA per (head, 128-query tile), the mirror image: Q and dO
@@ -37,7 +38,8 @@ namespace {
 __device__ uint32_t g_error_word;
 
 constexpr int kBT = 128;            // tile edge: rows of every tile, keys / queries per tile
-constexpr int kBwdThreads = 192;    // warps 0-3 elementwise, warp 4 MMA, warp 5 TMA
+constexpr int kBwdThreads = 320;    // warps 0-7 elementwise, warp 8 MMA, warp 9 TMA
+constexpr int kMmaWarp = 8, kTmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 
 template <int D, bool KV>
@@ -108,9 +110,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
 }
 
 // Work unit of a CTA.  dKdV: key block kb of head bh, query tiles j0 .. nt-1
-// (causal: from the diagonal tile on; ascending kb = longest first).  dQ:
-// query tile qt of head bh, key tiles 0 .. j_end-1 (causal: up to the
-// diagonal; descending qt = longest first).
+// (causal: from the diagonal tile on).  dQ: query tile qt of head bh, key
+// tiles 0 .. j_end-1 (causal: up to the diagonal).  Causal grids run the
+// longest units first (ascending kb, descending qt); otherwise head-major.
 struct BwdTask {
     int bh, blk, j0, n;
 };
@@ -119,13 +121,19 @@ template <bool KV, bool CAUSAL>
 __device__ __forceinline__ BwdTask bwd_task(const BwdArgs& a) {
     BwdTask t;
     const int idx = blockIdx.x;
-    t.bh = idx % a.BH;
+    if (CAUSAL) {
+        // longest first: across heads, by block
+        t.bh = idx % a.BH;
+        t.blk = KV ? idx / a.BH : a.num_tiles - 1 - idx / a.BH;
+    } else {
+        // head-major: CTAs running together stream the same head's tiles (L2 reuse)
+        t.bh = idx / a.num_tiles;
+        t.blk = idx % a.num_tiles;
+    }
     if (KV) {
-        t.blk = idx / a.BH;
         t.j0 = CAUSAL ? t.blk : 0;
         t.n = a.num_tiles - t.j0;
     } else {
-        t.blk = CAUSAL ? a.num_tiles - 1 - idx / a.BH : idx / a.BH;
         t.j0 = 0;
         t.n = CAUSAL ? t.blk + 1 : a.num_tiles;
     }
@@ -151,12 +159,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             mbar_init(&bars.empty[s], 1);
         }
         mbar_init(bars.s_full, 1);
-        mbar_init(bars.p_full, 4);
+        mbar_init(bars.p_full, 8);
         mbar_init(bars.done, 1);
         *bars.abort_flag = 0u;
         fence_barrier_init();
     }
-    if (warp == 4) {
+    if (warp == kMmaWarp) {
         tmem_alloc(bars.tmem_slot, kTmemCols);
         tmem_relinquish();
     }
@@ -170,7 +178,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
     const int blk0 = tk.blk * kBT;  // first row of the resident tiles
     const int kvh = tk.bh;          // multi-head: K/V head = query head
 
-    if (warp == 5) {
+    if (warp == kTmaWarp) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             const CUtensorMap* outer1 = KV ? &a.tmap_k : &a.tmap_q;
@@ -219,7 +227,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                 mbar_wait_bounded(bars.outer_full, 0u, nullptr, &g_error_word, a.timeout_ns);
             }
         }
-    } else if (warp == 4) {
+    } else if (warp == kMmaWarp) {
         // ---------------- MMA issue (one elected lane) ----------------
         constexpr uint32_t kIdescS = idesc_f16_f32(kBT, kBT, BF16 ? 1u : 0u, 0u, 0u);
         constexpr uint32_t kIdescAcc = idesc_f16_f32(kBT, D, BF16 ? 1u : 0u, 0u, 1u);
@@ -255,17 +263,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             if (!ok) break;
             tc_fence_after();
             if (elect_one_sync()) {
-                // acc (+)= (16-bit tile in TMEM, 8 columns per 16 rows of the
-                // inner tile) x inner tile as an MN-major operand.
+                // acc (+)= (16-bit tile in TMEM) x inner tile as an MN-major
+                // operand.  The 16-bit tile holds inner rows 0-63 packed in
+                // columns [0,32) and rows 64-127 in [64,96) (8 columns per 16 rows).
 #pragma unroll
                 for (int kk = 0; kk < kBT / 16; ++kk) {
                     const uint64_t boff = (kk * 16 * 128) >> 4;
                     const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                    const uint32_t acol = (kk / 4) * 64 + (kk % 4) * 8;
                     if (KV) {
-                        mma_ts(t_acc1, t_s + kk * 8, mnmaj + (inner2_s >> 4) + boff, kIdescAcc, acc);   // dV += P^T dO
-                        mma_ts(t_acc2, t_dp + kk * 8, mnmaj + (inner1_s >> 4) + boff, kIdescAcc, acc);  // dK += dS^T Q
+                        mma_ts(t_acc1, t_s + acol, mnmaj + (inner2_s >> 4) + boff, kIdescAcc, acc);   // dV += P^T dO
+                        mma_ts(t_acc2, t_dp + acol, mnmaj + (inner1_s >> 4) + boff, kIdescAcc, acc);  // dK += dS^T Q
                     } else {
-                        mma_ts(t_acc1, t_dp + kk * 8, mnmaj + (inner1_s >> 4) + boff, kIdescAcc, acc);  // dQ += dS K
+                        mma_ts(t_acc1, t_dp + acol, mnmaj + (inner1_s >> 4) + boff, kIdescAcc, acc);  // dQ += dS K
                     }
                 }
                 mma_commit(&bars.empty[s]);
@@ -275,10 +285,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         if (elect_one_sync()) mma_commit(bars.done);  // fires once every MMA above has completed
         __syncwarp();
     } else {
-        // ---------------- elementwise warps 0-3: thread = TMEM lane = resident row ----------------
-        const int r = warp * 32 + lane;
+        // ---------------- elementwise warps 0-7 ----------------
+        // Warps w and w+4 share TMEM lane quarter w % 4 (thread = lane =
+        // resident row); warp w < 4 takes columns [0,64) of S and dP, warp
+        // w + 4 columns [64,128), and each packs its 16-bit results into the
+        // first half of its own column range.
+        const int quarter = warp % 4, half = warp / 4;
+        const int r = quarter * 32 + lane;
         const int row = blk0 + r;  // KV: key index; dQ: query index
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const int c0 = half * 64;  // first column of this warp
         float lse2_r = 0.f, delta_r = 0.f;
         if (!KV) {
             const float* stats = a.ws + static_cast<int64_t>(tk.bh) * 2 * a.Npad + row;
@@ -297,11 +313,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             const float* lse2s = reinterpret_cast<const float*>(smem + L::kRing + s * L::kStageBytes + 2 * L::kTile);
             const float* deltas = lse2s + kBT;
             const bool diag = CAUSAL && j == tk.blk;
-#pragma unroll 1
-            for (int c = 0; c < kBT / 32; ++c) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
                 uint32_t sv[32], dpv[32];
-                tmem_ld32(t_s + lane_off + c * 32, sv);
-                tmem_ld32(t_dp + lane_off + c * 32, dpv);
+                tmem_ld32(t_s + lane_off + c0 + c * 32, sv);
+                tmem_ld32(t_dp + lane_off + c0 + c * 32, dpv);
                 tmem_wait_ld();
                 reg_fence(sv);
                 reg_fence(dpv);
@@ -311,7 +327,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                     float p[2], ds[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const int col = c * 32 + e + u;  // KV: query j*128+col; dQ: key j*128+col
+                        const int col = c0 + c * 32 + e + u;  // KV: query j*128+col; dQ: key j*128+col
                         const float lse2 = KV ? lse2s[col] : lse2_r;
                         const float dlt = KV ? deltas[col] : delta_r;
                         float pv = ex2_approx(__uint_as_float(sv[e + u]) * a.sl2 - lse2);
@@ -327,8 +343,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                     pk[e / 2] = pack16(p[0], p[1], BF16);
                     dsk[e / 2] = pack16(ds[0], ds[1], BF16);
                 }
-                if (KV) tmem_st16(t_s + lane_off + c * 16, pk);
-                tmem_st16(t_dp + lane_off + c * 16, dsk);
+                if (KV) tmem_st16(t_s + lane_off + c0 + c * 16, pk);
+                tmem_st16(t_dp + lane_off + c0 + c * 16, dsk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -336,6 +352,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             if (lane == 0) mbar_arrive(bars.p_full);
         }
         // ---------------- epilogue: accumulators -> 16-bit rows ----------------
+        // Each warp converts half of the D columns of its 32 rows.
         const bool fin = warp_wait(bars.done, 0u, nullptr, a.timeout_ns);
         tc_fence_after();
         const int64_t out_row = static_cast<int64_t>(tk.bh) * a.N + row;
@@ -347,7 +364,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             void* base = KV ? (acc == 0 ? a.dv : a.dk) : a.dq;
             uint8_t* orow = reinterpret_cast<uint8_t*>(base) + out_row * D * 2;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
                 uint32_t v[32];
                 tmem_ld32(tacc + c * 32, v);  // warp-collective: every lane, whatever its row
                 tmem_wait_ld();
@@ -367,7 +384,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
