@@ -42,25 +42,40 @@ constexpr int kBwdThreads = 320;    // warps 0-7 elementwise, warp 8 MMA, warp 9
 constexpr int kMmaWarp = 8, kTmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 
+// Shared memory: the two resident tiles, then ring A and ring B.
+//   dK/dV: ring A slots hold a whole inner tile pair (Q, dO) and its 128
+//          queries' LSE*log2e and Delta; ring B is empty (Q and dO are both
+//          read until the tile's accumulating products).
+//   dQ:    ring A holds K tiles, ring B V tiles: V is free once dP is done,
+//          earlier than K (read again by dQ += dS K), so the two rings are
+//          released separately and K gets the deeper one.
 template <int D, bool KV>
 struct BwdLayout {
     static constexpr int kTile = kBT * D * 2;               // one [128][D] 16-bit tile
     static constexpr int kStats = KV ? 2 * kBT * 4 : 0;     // LSE*log2e and Delta of 128 queries
-    static constexpr int kStages = D == 128 ? 2 : 4;
-    static constexpr int kStageBytes = (2 * kTile + kStats + 1023) / 1024 * 1024;
+    static constexpr int kSA = KV ? (D == 128 ? 2 : 4) : (D == 128 ? 3 : 4);
+    static constexpr int kSB = KV ? 0 : (D == 128 ? 2 : 4);
+    static constexpr int kSBm = kSB > 0 ? kSB : 1;          // divisor for ring B indices
+    static constexpr int kSlotA = KV ? (2 * kTile + kStats + 1023) / 1024 * 1024 : kTile;
+    static constexpr int kSlotB = kTile;
     static constexpr int kOuter = 0;                        // two resident tiles
-    static constexpr int kRing = 2 * kTile;
-    static constexpr int kBar = kRing + kStages * kStageBytes;
-    // barriers: outer_full, full[S], empty[S], s_full, p_full, done; abort flag; TMEM slot
-    static constexpr int kBytes = kBar + (4 + 2 * kStages) * 8 + 16;
+    static constexpr int kRingA = 2 * kTile;
+    static constexpr int kRingB = kRingA + kSA * kSlotA;
+    static constexpr int kBar = kRingB + kSB * kSlotB;
+    // barriers: outer_full, fullA/emptyA[SA], fullB/emptyB[SB], s_full, dp_free,
+    // p_full, done; abort flag; TMEM slot
+    static constexpr int kBytes = kBar + (5 + 2 * kSA + 2 * kSB) * 8 + 16;
     static_assert(kBytes <= 227 * 1024, "shared memory");
 };
 
 struct BwdBars {
     uint64_t* outer_full;
-    uint64_t* full;
-    uint64_t* empty;
+    uint64_t* full_a;
+    uint64_t* empty_a;
+    uint64_t* full_b;
+    uint64_t* empty_b;
     uint64_t* s_full;
+    uint64_t* dp_free;
     uint64_t* p_full;
     uint64_t* done;
     uint32_t* abort_flag;
@@ -73,10 +88,13 @@ __device__ __forceinline__ BwdBars bwd_bars(uint8_t* smem) {
     BwdBars b;
     uint64_t* p = reinterpret_cast<uint64_t*>(smem + L::kBar);
     b.outer_full = p;
-    b.full = p + 1;
-    b.empty = b.full + L::kStages;
-    b.s_full = b.empty + L::kStages;
-    b.p_full = b.s_full + 1;
+    b.full_a = p + 1;
+    b.empty_a = b.full_a + L::kSA;
+    b.full_b = b.empty_a + L::kSA;
+    b.empty_b = b.full_b + L::kSB;
+    b.s_full = b.empty_b + L::kSB;
+    b.dp_free = b.s_full + 1;
+    b.p_full = b.dp_free + 1;
     b.done = b.p_full + 1;
     b.abort_flag = reinterpret_cast<uint32_t*>(b.done + 1);
     b.tmem_slot = b.abort_flag + 1;
@@ -154,11 +172,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
 
     if (threadIdx.x == 0) {
         mbar_init(bars.outer_full, 1);
-        for (int s = 0; s < L::kStages; ++s) {
-            mbar_init(&bars.full[s], 1);
-            mbar_init(&bars.empty[s], 1);
+        for (int s = 0; s < L::kSA; ++s) {
+            mbar_init(&bars.full_a[s], 1);
+            mbar_init(&bars.empty_a[s], 1);
+        }
+        for (int s = 0; s < L::kSB; ++s) {
+            mbar_init(&bars.full_b[s], 1);
+            mbar_init(&bars.empty_b[s], 1);
         }
         mbar_init(bars.s_full, 1);
+        mbar_init(bars.dp_free, 8);
         mbar_init(bars.p_full, 8);
         mbar_init(bars.done, 1);
         *bars.abort_flag = 0u;
@@ -172,9 +195,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *bars.tmem_slot;
-    // TMEM columns: S (or S^T) [0,128), dP [128,256), acc1 [256,256+D), acc2 [256+D,256+2D).
-    // The 16-bit P and dS overwrite the first 64 columns of S and dP.
-    const uint32_t t_s = tmem, t_dp = tmem + 128, t_acc1 = tmem + 256, t_acc2 = tmem + 256 + D;
+    // TMEM columns.  dK/dV: S^T [0,128) (then the 16-bit P^T and dS^T, see
+    // below), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).  dQ: S in two
+    // buffers [0,128) and [128,256) (then the 16-bit dS), dP [256,384),
+    // dQ [384,384+D).  Within a 32-column chunk of S the 16-bit results go to
+    // its first 16 columns (P, or dS for dQ) and, for dK/dV, dS^T to the next 16.
+    const uint32_t t_s = tmem;
+    const uint32_t t_dp = KV ? tmem + 128 : tmem + 256;
+    const uint32_t t_acc1 = KV ? tmem + 256 : tmem + 384;
+    const uint32_t t_acc2 = tmem + 256 + D;
     const int blk0 = tk.blk * kBT;  // first row of the resident tiles
     const int kvh = tk.bh;          // multi-head: K/V head = query head
 
@@ -191,37 +220,59 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                 tma_load_3d(smem + L::kOuter + L::kTile + at * kBT * 128, outer2, bars.outer_full, at * 64,
                             blk0, kvh);
             }
-            int issued = 0;
+            int issued_a = 0, issued_b = 0;
             bool ok = true;
             for (int it = 0; it < tk.n && ok; ++it) {
-                const int s = it % L::kStages;
-                if (it >= L::kStages) {
-                    ok = mbar_wait_bounded(&bars.empty[s], ((it / L::kStages) - 1) & 1u, bars.abort_flag,
+                const int row0 = (tk.j0 + it) * kBT;
+                const int sa = it % L::kSA;
+                if (it >= L::kSA) {
+                    ok = mbar_wait_bounded(&bars.empty_a[sa], ((it / L::kSA) - 1) & 1u, bars.abort_flag,
                                            &g_error_word, a.timeout_ns);
                     if (!ok) break;
                 }
-                const int row0 = (tk.j0 + it) * kBT;
-                uint8_t* st = smem + L::kRing + s * L::kStageBytes;
-                mbar_arrive_expect_tx(&bars.full[s], 2 * L::kTile + L::kStats);
+                uint8_t* st = smem + L::kRingA + sa * L::kSlotA;
+                mbar_arrive_expect_tx(&bars.full_a[sa], KV ? 2 * L::kTile + L::kStats : L::kTile);
                 for (int at = 0; at < D / 64; ++at) {
-                    tma_load_3d(st + at * kBT * 128, inner1, &bars.full[s], at * 64, row0, kvh);
-                    tma_load_3d(st + L::kTile + at * kBT * 128, inner2, &bars.full[s], at * 64, row0, kvh);
+                    tma_load_3d(st + at * kBT * 128, inner1, &bars.full_a[sa], at * 64, row0, kvh);
+                    if (KV)
+                        tma_load_3d(st + L::kTile + at * kBT * 128, inner2, &bars.full_a[sa], at * 64, row0, kvh);
                 }
                 if (KV) {
                     const float* stats = a.ws + static_cast<int64_t>(tk.bh) * 2 * a.Npad + row0;
-                    bulk_load(st + 2 * L::kTile, stats, kBT * 4, &bars.full[s]);
-                    bulk_load(st + 2 * L::kTile + kBT * 4, stats + a.Npad, kBT * 4, &bars.full[s]);
+                    bulk_load(st + 2 * L::kTile, stats, kBT * 4, &bars.full_a[sa]);
+                    bulk_load(st + 2 * L::kTile + kBT * 4, stats + a.Npad, kBT * 4, &bars.full_a[sa]);
                 }
-                ++issued;
+                ++issued_a;
+                if (!KV) {
+                    const int sb = it % L::kSBm;
+                    if (it >= L::kSB) {
+                        ok = mbar_wait_bounded(&bars.empty_b[sb], ((it / L::kSBm) - 1) & 1u, bars.abort_flag,
+                                               &g_error_word, a.timeout_ns);
+                        if (!ok) break;
+                    }
+                    uint8_t* sv = smem + L::kRingB + sb * L::kSlotB;
+                    mbar_arrive_expect_tx(&bars.full_b[sb], L::kTile);
+                    for (int at = 0; at < D / 64; ++at)
+                        tma_load_3d(sv + at * kBT * 128, inner2, &bars.full_b[sb], at * 64, row0, kvh);
+                    ++issued_b;
+                }
             }
             if (!ok) {
                 // Let the copies already started land before the CTA leaves.
-                for (int s = 0; s < L::kStages; ++s) {
+                for (int s = 0; s < L::kSA; ++s) {
                     int last = -1;
-                    for (int i = 0; i < issued; ++i)
-                        if (i % L::kStages == s) last = i;
+                    for (int i = 0; i < issued_a; ++i)
+                        if (i % L::kSA == s) last = i;
                     if (last >= 0)
-                        mbar_wait_bounded(&bars.full[s], (last / L::kStages) & 1u, nullptr, &g_error_word,
+                        mbar_wait_bounded(&bars.full_a[s], (last / L::kSA) & 1u, nullptr, &g_error_word,
+                                          a.timeout_ns);
+                }
+                for (int s = 0; s < L::kSB; ++s) {
+                    int last = -1;
+                    for (int i = 0; i < issued_b; ++i)
+                        if (i % L::kSBm == s) last = i;
+                    if (last >= 0)
+                        mbar_wait_bounded(&bars.full_b[s], (last / L::kSBm) & 1u, nullptr, &g_error_word,
                                           a.timeout_ns);
                 }
                 mbar_wait_bounded(bars.outer_full, 0u, nullptr, &g_error_word, a.timeout_ns);
@@ -229,56 +280,108 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issue (one elected lane) ----------------
+        // Per inner tile it: S(it) and dP(it) -> s_full; the elementwise warps
+        // load dP(it) and release its columns (dp_free), so dP(it+1) (and for
+        // dQ, S(it+1) into the other buffer) run while they work; once the
+        // 16-bit P/dS are in TMEM (p_full) the accumulating products follow,
+        // then (dK/dV) S(it+1) into the single S region.
         constexpr uint32_t kIdescS = idesc_f16_f32(kBT, kBT, BF16 ? 1u : 0u, 0u, 0u);
         constexpr uint32_t kIdescAcc = idesc_f16_f32(kBT, D, BF16 ? 1u : 0u, 0u, 1u);
         const uint64_t kmaj = smem_desc_sw128(0u, 16u, 1024u);
         const uint64_t mnmaj = smem_desc_sw128(0u, kBT * 128u, 1024u);
         const uint32_t outer1_s = smem_u32(smem + L::kOuter), outer2_s = outer1_s + L::kTile;
-        bool ok = warp_wait(bars.outer_full, 0u, bars.abort_flag, a.timeout_ns);
-        for (int it = 0; it < tk.n && ok; ++it) {
-            const int s = it % L::kStages;
-            ok = warp_wait(&bars.full[s], (it / L::kStages) & 1u, bars.abort_flag, a.timeout_ns);
-            if (!ok) break;
+        auto inner1 = [&](int it) { return smem_u32(smem + L::kRingA + (it % L::kSA) * L::kSlotA); };
+        auto inner2 = [&](int it) {
+            return KV ? inner1(it) + L::kTile : smem_u32(smem + L::kRingB + (it % L::kSBm) * L::kSlotB);
+        };
+        auto s_buf = [&](int it) { return KV ? t_s : t_s + 128u * static_cast<uint32_t>(it & 1); };
+        // S = outer1 inner1^T, dP = outer2 inner2^T: both operands K-major over D.
+        auto issue_s = [&](int it) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = ((kk / 4) * (kBT * 128) + (kk % 4) * 32) >> 4;
+                mma_ss(s_buf(it), kmaj + (outer1_s >> 4) + off, kmaj + (inner1(it) >> 4) + off, kIdescS,
+                       kk > 0 ? 1u : 0u);
+            }
+        };
+        auto issue_dp = [&](int it) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = ((kk / 4) * (kBT * 128) + (kk % 4) * 32) >> 4;
+                mma_ss(t_dp, kmaj + (outer2_s >> 4) + off, kmaj + (inner2(it) >> 4) + off, kIdescS,
+                       kk > 0 ? 1u : 0u);
+            }
+        };
+        // acc (+)= (16-bit tile in TMEM, 8 columns per 16 inner rows) x inner
+        // tile as an MN-major operand.
+        auto issue_acc = [&](int it) {
+            const uint32_t in1 = inner1(it), in2 = inner2(it);
+#pragma unroll
+            for (int kk = 0; kk < kBT / 16; ++kk) {
+                const uint64_t boff = (kk * 16 * 128) >> 4;
+                const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                const uint32_t acol = (kk / 2) * 32 + (kk % 2) * 8;
+                if (KV) {
+                    mma_ts(t_acc1, t_s + acol, mnmaj + (in2 >> 4) + boff, kIdescAcc, acc);        // dV += P^T dO
+                    mma_ts(t_acc2, t_s + acol + 16, mnmaj + (in1 >> 4) + boff, kIdescAcc, acc);   // dK += dS^T Q
+                } else {
+                    mma_ts(t_acc1, s_buf(it) + acol, mnmaj + (in1 >> 4) + boff, kIdescAcc, acc);  // dQ += dS K
+                }
+            }
+        };
+        // wait for ring A (inner1; for dK/dV the whole stage) / ring B (dQ: V) of tile it
+        auto wait_a = [&](int it) {
+            const bool r = warp_wait(&bars.full_a[it % L::kSA], (it / L::kSA) & 1u, bars.abort_flag,
+                                     a.timeout_ns);
             tc_fence_after();
-            const uint32_t inner1_s = smem_u32(smem + L::kRing + s * L::kStageBytes);
-            const uint32_t inner2_s = inner1_s + L::kTile;
+            return r;
+        };
+        auto wait_b = [&](int it) {
+            if (KV) return true;
+            const bool r = warp_wait(&bars.full_b[it % L::kSBm], (it / L::kSBm) & 1u, bars.abort_flag,
+                                     a.timeout_ns);
+            tc_fence_after();
+            return r;
+        };
+        bool ok = warp_wait(bars.outer_full, 0u, bars.abort_flag, a.timeout_ns) && wait_a(0) && wait_b(0);
+        if (ok) {
             if (elect_one_sync()) {
-                // S = outer1 inner1^T and dP = outer2 inner2^T: both operands K-major over D.
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = ((kk / 4) * (kBT * 128) + (kk % 4) * 32) >> 4;
-                    mma_ss(t_s, kmaj + (outer1_s >> 4) + off, kmaj + (inner1_s >> 4) + off, kIdescS,
-                           kk > 0 ? 1u : 0u);
-                }
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = ((kk / 4) * (kBT * 128) + (kk % 4) * 32) >> 4;
-                    mma_ss(t_dp, kmaj + (outer2_s >> 4) + off, kmaj + (inner2_s >> 4) + off, kIdescS,
-                           kk > 0 ? 1u : 0u);
-                }
+                issue_s(0);
+                issue_dp(0);
                 mma_commit(bars.s_full);
+                if (!KV) mma_commit(&bars.empty_b[0]);
             }
             __syncwarp();
-            ok = warp_wait(bars.p_full, it & 1u, bars.abort_flag, a.timeout_ns);
-            if (!ok) break;
+        }
+        for (int it = 0; it < tk.n && ok; ++it) {
+            const bool more = it + 1 < tk.n;
+            if (!KV && more) {
+                if (!(ok = wait_a(it + 1))) break;
+                if (elect_one_sync()) issue_s(it + 1);
+                __syncwarp();
+            }
+            if (!(ok = warp_wait(bars.dp_free, it & 1u, bars.abort_flag, a.timeout_ns))) break;
             tc_fence_after();
-            if (elect_one_sync()) {
-                // acc (+)= (16-bit tile in TMEM) x inner tile as an MN-major
-                // operand.  The 16-bit tile holds inner rows 0-63 packed in
-                // columns [0,32) and rows 64-127 in [64,96) (8 columns per 16 rows).
-#pragma unroll
-                for (int kk = 0; kk < kBT / 16; ++kk) {
-                    const uint64_t boff = (kk * 16 * 128) >> 4;
-                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                    const uint32_t acol = (kk / 4) * 64 + (kk % 4) * 8;
-                    if (KV) {
-                        mma_ts(t_acc1, t_s + acol, mnmaj + (inner2_s >> 4) + boff, kIdescAcc, acc);   // dV += P^T dO
-                        mma_ts(t_acc2, t_dp + acol, mnmaj + (inner1_s >> 4) + boff, kIdescAcc, acc);  // dK += dS^T Q
-                    } else {
-                        mma_ts(t_acc1, t_dp + acol, mnmaj + (inner1_s >> 4) + boff, kIdescAcc, acc);  // dQ += dS K
+            if (more) {
+                if (!(ok = KV ? wait_a(it + 1) : wait_b(it + 1))) break;
+                if (elect_one_sync()) {
+                    issue_dp(it + 1);
+                    if (!KV) {
+                        mma_commit(bars.s_full);
+                        mma_commit(&bars.empty_b[(it + 1) % L::kSBm]);  // V slot free once dP is done
                     }
                 }
-                mma_commit(&bars.empty[s]);
+                __syncwarp();
+            }
+            if (!(ok = warp_wait(bars.p_full, it & 1u, bars.abort_flag, a.timeout_ns))) break;
+            tc_fence_after();
+            if (elect_one_sync()) {
+                issue_acc(it);
+                mma_commit(&bars.empty_a[it % L::kSA]);
+                if (KV && more) {
+                    issue_s(it + 1);
+                    mma_commit(bars.s_full);
+                }
             }
             __syncwarp();
         }
@@ -288,8 +391,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         // ---------------- elementwise warps 0-7 ----------------
         // Warps w and w+4 share TMEM lane quarter w % 4 (thread = lane =
         // resident row); warp w < 4 takes columns [0,64) of S and dP, warp
-        // w + 4 columns [64,128), and each packs its 16-bit results into the
-        // first half of its own column range.
+        // w + 4 columns [64,128), and each writes its 16-bit results into the
+        // S columns it has already read.
         const int quarter = warp % 4, half = warp / 4;
         const int r = quarter * 32 + lane;
         const int row = blk0 + r;  // KV: key index; dQ: query index
@@ -304,23 +407,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         bool ok = true;
         for (int it = 0; it < tk.n && ok; ++it) {
             const int j = tk.j0 + it;
-            const int s = it % L::kStages;
+            const int s = it % L::kSA;
             ok = warp_wait(bars.s_full, it & 1u, bars.abort_flag, a.timeout_ns);
             if (KV && ok)  // the stage's statistics: this phase is complete and not yet refilled
-                ok = warp_wait(&bars.full[s], (it / L::kStages) & 1u, bars.abort_flag, a.timeout_ns);
+                ok = warp_wait(&bars.full_a[s], (it / L::kSA) & 1u, bars.abort_flag, a.timeout_ns);
             if (!ok) break;
             tc_fence_after();
-            const float* lse2s = reinterpret_cast<const float*>(smem + L::kRing + s * L::kStageBytes + 2 * L::kTile);
+            const float* lse2s = reinterpret_cast<const float*>(smem + L::kRingA + s * L::kSlotA + 2 * L::kTile);
             const float* deltas = lse2s + kBT;
             const bool diag = CAUSAL && j == tk.blk;
+            const uint32_t sb = (KV ? t_s : t_s + 128u * static_cast<uint32_t>(it & 1)) + lane_off + c0;
+            // dP first, in full, so that its columns can be handed back at once.
+            uint32_t dpv[2][32], sv[32];
+            tmem_ld32(t_dp + lane_off + c0, dpv[0]);
+            tmem_ld32(t_dp + lane_off + c0 + 32, dpv[1]);
+            tmem_ld32(sb, sv);
+            tmem_wait_ld();
+            reg_fence(dpv[0]);
+            reg_fence(dpv[1]);
+            reg_fence(sv);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.dp_free);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                uint32_t sv[32], dpv[32];
-                tmem_ld32(t_s + lane_off + c0 + c * 32, sv);
-                tmem_ld32(t_dp + lane_off + c0 + c * 32, dpv);
-                tmem_wait_ld();
-                reg_fence(sv);
-                reg_fence(dpv);
+                if (c == 1) {
+                    tmem_ld32(sb + 32, sv);
+                    tmem_wait_ld();
+                    reg_fence(sv);
+                }
                 uint32_t pk[16], dsk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
@@ -338,13 +453,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                             if (key >= a.N || (diag && col > r)) pv = 0.f;
                         }
                         p[u] = pv;
-                        ds[u] = pv * (__uint_as_float(dpv[e + u]) - dlt);
+                        ds[u] = pv * (__uint_as_float(dpv[c][e + u]) - dlt);
                     }
                     pk[e / 2] = pack16(p[0], p[1], BF16);
                     dsk[e / 2] = pack16(ds[0], ds[1], BF16);
                 }
-                if (KV) tmem_st16(t_s + lane_off + c0 + c * 16, pk);
-                tmem_st16(t_dp + lane_off + c0 + c * 16, dsk);
+                // Only columns of this chunk, already read, are overwritten.
+                if (KV) {
+                    tmem_st16(sb + c * 32, pk);
+                    tmem_st16(sb + c * 32 + 16, dsk);
+                } else {
+                    tmem_st16(sb + c * 32, dsk);
+                }
             }
             tmem_wait_st();
             tc_fence_before();
