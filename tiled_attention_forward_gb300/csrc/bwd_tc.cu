@@ -43,28 +43,32 @@ constexpr int kMmaWarp = 8, kTmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 
 // Shared memory: the two resident tiles, then ring A and ring B.
-//   dK/dV: ring A slots hold a whole inner tile pair (Q, dO) and its 128
+//   dK/dV: ring A slots hold a 64-query inner tile pair (Q, dO) and those
 //          queries' LSE*log2e and Delta; ring B is empty (Q and dO are both
 //          read until the tile's accumulating products).
 //   dQ:    ring A holds K tiles, ring B V tiles: V is free once dP is done,
 //          earlier than K (read again by dQ += dS K), so the two rings are
 //          released separately and K gets the deeper one.
+constexpr int kBQ = 64;  // queries per inner tile of the dK/dV kernel
+
 template <int D, bool KV>
 struct BwdLayout {
     static constexpr int kTile = kBT * D * 2;               // one [128][D] 16-bit tile
-    static constexpr int kStats = KV ? 2 * kBT * 4 : 0;     // LSE*log2e and Delta of 128 queries
-    static constexpr int kSA = KV ? (D == 128 ? 2 : 4) : (D == 128 ? 3 : 4);
+    static constexpr int kTileIn = KV ? kBQ * D * 2 : kTile; // one streamed inner tile
+    static constexpr int kAtomIn = KV ? kBQ * 128 : kBT * 128; // bytes of one 64-wide swizzle atom of it
+    static constexpr int kStats = KV ? 2 * kBQ * 4 : 0;     // LSE*log2e and Delta of the tile's queries
+    static constexpr int kSA = KV ? (D == 128 ? 4 : 6) : (D == 128 ? 3 : 4);
     static constexpr int kSB = KV ? 0 : (D == 128 ? 2 : 4);
     static constexpr int kSBm = kSB > 0 ? kSB : 1;          // divisor for ring B indices
-    static constexpr int kSlotA = KV ? (2 * kTile + kStats + 1023) / 1024 * 1024 : kTile;
+    static constexpr int kSlotA = KV ? (2 * kTileIn + kStats + 1023) / 1024 * 1024 : kTile;
     static constexpr int kSlotB = kTile;
     static constexpr int kOuter = 0;                        // two resident tiles
     static constexpr int kRingA = 2 * kTile;
     static constexpr int kRingB = kRingA + kSA * kSlotA;
     static constexpr int kBar = kRingB + kSB * kSlotB;
-    // barriers: outer_full, fullA/emptyA[SA], fullB/emptyB[SB], s_full, dp_free,
-    // p_full, done; abort flag; TMEM slot
-    static constexpr int kBytes = kBar + (5 + 2 * kSA + 2 * kSB) * 8 + 16;
+    // barriers: outer_full, fullA/emptyA[SA], fullB/emptyB[SB], s_full[2],
+    // dp_free, p_full[2], done; abort flag; TMEM slot
+    static constexpr int kBytes = kBar + (7 + 2 * kSA + 2 * kSB) * 8 + 16;
     static_assert(kBytes <= 227 * 1024, "shared memory");
 };
 
@@ -92,10 +96,10 @@ __device__ __forceinline__ BwdBars bwd_bars(uint8_t* smem) {
     b.empty_a = b.full_a + L::kSA;
     b.full_b = b.empty_a + L::kSA;
     b.empty_b = b.full_b + L::kSB;
-    b.s_full = b.empty_b + L::kSB;
-    b.dp_free = b.s_full + 1;
-    b.p_full = b.dp_free + 1;
-    b.done = b.p_full + 1;
+    b.s_full = b.empty_b + L::kSB;   // [2]: one per S buffer / tile parity
+    b.dp_free = b.s_full + 2;
+    b.p_full = b.dp_free + 1;        // [2]
+    b.done = b.p_full + 2;
     b.abort_flag = reinterpret_cast<uint32_t*>(b.done + 1);
     b.tmem_slot = b.abort_flag + 1;
     return b;
@@ -127,8 +131,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
                                                      timeout_ns));
 }
 
-// Work unit of a CTA.  dKdV: key block kb of head bh, query tiles j0 .. nt-1
-// (causal: from the diagonal tile on).  dQ: query tile qt of head bh, key
+// Work unit of a CTA.  dKdV: key block kb of head bh, 64-query tiles
+// j0 .. 2*nt-1 (causal: from the first tile that meets the block's diagonal).  dQ: query tile qt of head bh, key
 // tiles 0 .. j_end-1 (causal: up to the diagonal).  Causal grids run the
 // longest units first (ascending kb, descending qt); otherwise head-major.
 struct BwdTask {
@@ -148,9 +152,9 @@ __device__ __forceinline__ BwdTask bwd_task(const BwdArgs& a) {
         t.bh = idx / a.num_tiles;
         t.blk = idx % a.num_tiles;
     }
-    if (KV) {
-        t.j0 = CAUSAL ? t.blk : 0;
-        t.n = a.num_tiles - t.j0;
+    if (KV) {  // 64-query inner tiles: two per 128-key block
+        t.j0 = CAUSAL ? 2 * t.blk : 0;
+        t.n = 2 * a.num_tiles - t.j0;
     } else {
         t.j0 = 0;
         t.n = CAUSAL ? t.blk + 1 : a.num_tiles;
@@ -180,9 +184,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             mbar_init(&bars.full_b[s], 1);
             mbar_init(&bars.empty_b[s], 1);
         }
-        mbar_init(bars.s_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.s_full[i], 1);
+            mbar_init(&bars.p_full[i], 8);
+        }
         mbar_init(bars.dp_free, 8);
-        mbar_init(bars.p_full, 8);
         mbar_init(bars.done, 1);
         *bars.abort_flag = 0u;
         fence_barrier_init();
@@ -195,13 +201,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *bars.tmem_slot;
-    // TMEM columns.  dK/dV: S^T [0,128) (then the 16-bit P^T and dS^T, see
-    // below), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).  dQ: S in two
+    // TMEM columns.  dK/dV: two buffers b = tile parity, S^T_b [128b,128b+64)
+    // and dP^T_b [128b+64,128b+128) (64 queries each; the 16-bit P^T and dS^T
+    // overwrite S^T_b), dV [256,256+D), dK [256+D,256+2D).  dQ: S in two
     // buffers [0,128) and [128,256) (then the 16-bit dS), dP [256,384),
     // dQ [384,384+D).  Within a 32-column chunk of S the 16-bit results go to
     // its first 16 columns (P, or dS for dQ) and, for dK/dV, dS^T to the next 16.
     const uint32_t t_s = tmem;
-    const uint32_t t_dp = KV ? tmem + 128 : tmem + 256;
+    const uint32_t t_dp = KV ? tmem + 64 : tmem + 256;   // dK/dV: + 128 * b
     const uint32_t t_acc1 = KV ? tmem + 256 : tmem + 384;
     const uint32_t t_acc2 = tmem + 256 + D;
     const int blk0 = tk.blk * kBT;  // first row of the resident tiles
@@ -212,8 +219,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         if (lane == 0) {
             const CUtensorMap* outer1 = KV ? &a.tmap_k : &a.tmap_q;
             const CUtensorMap* outer2 = KV ? &a.tmap_v : &a.tmap_do;
-            const CUtensorMap* inner1 = KV ? &a.tmap_q : &a.tmap_k;
-            const CUtensorMap* inner2 = KV ? &a.tmap_do : &a.tmap_v;
+            const CUtensorMap* inner1 = KV ? &a.tmap_q64 : &a.tmap_k;
+            const CUtensorMap* inner2 = KV ? &a.tmap_do64 : &a.tmap_v;
             mbar_arrive_expect_tx(bars.outer_full, 2 * L::kTile);
             for (int at = 0; at < D / 64; ++at) {
                 tma_load_3d(smem + L::kOuter + at * kBT * 128, outer1, bars.outer_full, at * 64, blk0, kvh);
@@ -223,7 +230,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             int issued_a = 0, issued_b = 0;
             bool ok = true;
             for (int it = 0; it < tk.n && ok; ++it) {
-                const int row0 = (tk.j0 + it) * kBT;
+                const int row0 = (tk.j0 + it) * (KV ? kBQ : kBT);
                 const int sa = it % L::kSA;
                 if (it >= L::kSA) {
                     ok = mbar_wait_bounded(&bars.empty_a[sa], ((it / L::kSA) - 1) & 1u, bars.abort_flag,
@@ -231,16 +238,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                     if (!ok) break;
                 }
                 uint8_t* st = smem + L::kRingA + sa * L::kSlotA;
-                mbar_arrive_expect_tx(&bars.full_a[sa], KV ? 2 * L::kTile + L::kStats : L::kTile);
+                mbar_arrive_expect_tx(&bars.full_a[sa], KV ? 2 * L::kTileIn + L::kStats : L::kTile);
                 for (int at = 0; at < D / 64; ++at) {
-                    tma_load_3d(st + at * kBT * 128, inner1, &bars.full_a[sa], at * 64, row0, kvh);
+                    tma_load_3d(st + at * L::kAtomIn, inner1, &bars.full_a[sa], at * 64, row0, kvh);
                     if (KV)
-                        tma_load_3d(st + L::kTile + at * kBT * 128, inner2, &bars.full_a[sa], at * 64, row0, kvh);
+                        tma_load_3d(st + L::kTileIn + at * L::kAtomIn, inner2, &bars.full_a[sa], at * 64, row0,
+                                    kvh);
                 }
                 if (KV) {
                     const float* stats = a.ws + static_cast<int64_t>(tk.bh) * 2 * a.Npad + row0;
-                    bulk_load(st + 2 * L::kTile, stats, kBT * 4, &bars.full_a[sa]);
-                    bulk_load(st + 2 * L::kTile + kBT * 4, stats + a.Npad, kBT * 4, &bars.full_a[sa]);
+                    bulk_load(st + 2 * L::kTileIn, stats, kBQ * 4, &bars.full_a[sa]);
+                    bulk_load(st + 2 * L::kTileIn + kBQ * 4, stats + a.Npad, kBQ * 4, &bars.full_a[sa]);
                 }
                 ++issued_a;
                 if (!KV) {
@@ -280,56 +288,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issue (one elected lane) ----------------
-        // Per inner tile it: S(it) and dP(it) -> s_full; the elementwise warps
-        // load dP(it) and release its columns (dp_free), so dP(it+1) (and for
-        // dQ, S(it+1) into the other buffer) run while they work; once the
-        // 16-bit P/dS are in TMEM (p_full) the accumulating products follow,
-        // then (dK/dV) S(it+1) into the single S region.
-        constexpr uint32_t kIdescS = idesc_f16_f32(kBT, kBT, BF16 ? 1u : 0u, 0u, 0u);
+        // dK/dV: S^T and dP^T of 64-query tile it go to TMEM buffer it & 1;
+        // tiles it and it+1 are computed ahead, so while the elementwise warps
+        // work on one buffer the tensor pipe accumulates the previous tile and
+        // fills the other.  dQ: per key tile it, S(it) and dP(it) -> s_full;
+        // the elementwise warps load dP(it) and hand its columns back
+        // (dp_free), so dP(it+1) (and S(it+1), into the other buffer) run
+        // while they work, then dQ += dS K once the 16-bit dS is in TMEM.
+        constexpr uint32_t kIdescS = idesc_f16_f32(kBT, KV ? kBQ : kBT, BF16 ? 1u : 0u, 0u, 0u);
         constexpr uint32_t kIdescAcc = idesc_f16_f32(kBT, D, BF16 ? 1u : 0u, 0u, 1u);
+        constexpr int kInRows = KV ? kBQ : kBT;
         const uint64_t kmaj = smem_desc_sw128(0u, 16u, 1024u);
-        const uint64_t mnmaj = smem_desc_sw128(0u, kBT * 128u, 1024u);
+        const uint64_t mnmaj = smem_desc_sw128(0u, kInRows * 128u, 1024u);  // leading offset = slab size
         const uint32_t outer1_s = smem_u32(smem + L::kOuter), outer2_s = outer1_s + L::kTile;
         auto inner1 = [&](int it) { return smem_u32(smem + L::kRingA + (it % L::kSA) * L::kSlotA); };
         auto inner2 = [&](int it) {
-            return KV ? inner1(it) + L::kTile : smem_u32(smem + L::kRingB + (it % L::kSBm) * L::kSlotB);
+            return KV ? inner1(it) + L::kTileIn : smem_u32(smem + L::kRingB + (it % L::kSBm) * L::kSlotB);
         };
-        auto s_buf = [&](int it) { return KV ? t_s : t_s + 128u * static_cast<uint32_t>(it & 1); };
+        auto s_buf = [&](int it) { return t_s + 128u * static_cast<uint32_t>(it & 1); };
+        auto dp_buf = [&](int it) { return KV ? s_buf(it) + 64u : t_dp; };
         // S = outer1 inner1^T, dP = outer2 inner2^T: both operands K-major over D.
         auto issue_s = [&](int it) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t off = ((kk / 4) * (kBT * 128) + (kk % 4) * 32) >> 4;
-                mma_ss(s_buf(it), kmaj + (outer1_s >> 4) + off, kmaj + (inner1(it) >> 4) + off, kIdescS,
+                const uint64_t off_a = ((kk / 4) * (kBT * 128) + (kk % 4) * 32) >> 4;
+                const uint64_t off_b = ((kk / 4) * L::kAtomIn + (kk % 4) * 32) >> 4;
+                mma_ss(s_buf(it), kmaj + (outer1_s >> 4) + off_a, kmaj + (inner1(it) >> 4) + off_b, kIdescS,
                        kk > 0 ? 1u : 0u);
             }
         };
         auto issue_dp = [&](int it) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t off = ((kk / 4) * (kBT * 128) + (kk % 4) * 32) >> 4;
-                mma_ss(t_dp, kmaj + (outer2_s >> 4) + off, kmaj + (inner2(it) >> 4) + off, kIdescS,
+                const uint64_t off_a = ((kk / 4) * (kBT * 128) + (kk % 4) * 32) >> 4;
+                const uint64_t off_b = ((kk / 4) * L::kAtomIn + (kk % 4) * 32) >> 4;
+                mma_ss(dp_buf(it), kmaj + (outer2_s >> 4) + off_a, kmaj + (inner2(it) >> 4) + off_b, kIdescS,
                        kk > 0 ? 1u : 0u);
             }
         };
         // acc (+)= (16-bit tile in TMEM, 8 columns per 16 inner rows) x inner
-        // tile as an MN-major operand.
+        // tile as an MN-major operand (16 inner rows = 2048 bytes).
         auto issue_acc = [&](int it) {
             const uint32_t in1 = inner1(it), in2 = inner2(it);
 #pragma unroll
-            for (int kk = 0; kk < kBT / 16; ++kk) {
+            for (int kk = 0; kk < kInRows / 16; ++kk) {
                 const uint64_t boff = (kk * 16 * 128) >> 4;
                 const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
                 const uint32_t acol = (kk / 2) * 32 + (kk % 2) * 8;
                 if (KV) {
-                    mma_ts(t_acc1, t_s + acol, mnmaj + (in2 >> 4) + boff, kIdescAcc, acc);        // dV += P^T dO
-                    mma_ts(t_acc2, t_s + acol + 16, mnmaj + (in1 >> 4) + boff, kIdescAcc, acc);   // dK += dS^T Q
+                    mma_ts(t_acc1, s_buf(it) + acol, mnmaj + (in2 >> 4) + boff, kIdescAcc, acc);       // dV += P^T dO
+                    mma_ts(t_acc2, s_buf(it) + acol + 16, mnmaj + (in1 >> 4) + boff, kIdescAcc, acc);  // dK += dS^T Q
                 } else {
-                    mma_ts(t_acc1, s_buf(it) + acol, mnmaj + (in1 >> 4) + boff, kIdescAcc, acc);  // dQ += dS K
+                    mma_ts(t_acc1, s_buf(it) + acol, mnmaj + (in1 >> 4) + boff, kIdescAcc, acc);       // dQ += dS K
                 }
             }
         };
-        // wait for ring A (inner1; for dK/dV the whole stage) / ring B (dQ: V) of tile it
+        // wait for ring A (inner1; for dK/dV the whole slot) / ring B (dQ: V) of tile it
         auto wait_a = [&](int it) {
             const bool r = warp_wait(&bars.full_a[it % L::kSA], (it / L::kSA) & 1u, bars.abort_flag,
                                      a.timeout_ns);
@@ -343,56 +357,80 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             tc_fence_after();
             return r;
         };
-        bool ok = warp_wait(bars.outer_full, 0u, bars.abort_flag, a.timeout_ns) && wait_a(0) && wait_b(0);
-        if (ok) {
-            if (elect_one_sync()) {
-                issue_s(0);
-                issue_dp(0);
-                mma_commit(bars.s_full);
-                if (!KV) mma_commit(&bars.empty_b[0]);
-            }
-            __syncwarp();
-        }
-        for (int it = 0; it < tk.n && ok; ++it) {
-            const bool more = it + 1 < tk.n;
-            if (!KV && more) {
-                if (!(ok = wait_a(it + 1))) break;
-                if (elect_one_sync()) issue_s(it + 1);
+        bool ok = warp_wait(bars.outer_full, 0u, bars.abort_flag, a.timeout_ns);
+        if (KV) {
+            for (int t = 0; t < 2 && t < tk.n && ok; ++t) {
+                if (!(ok = wait_a(t))) break;
+                if (elect_one_sync()) {
+                    issue_s(t);
+                    issue_dp(t);
+                    mma_commit(&bars.s_full[t]);
+                }
                 __syncwarp();
             }
-            if (!(ok = warp_wait(bars.dp_free, it & 1u, bars.abort_flag, a.timeout_ns))) break;
-            tc_fence_after();
-            if (more) {
-                if (!(ok = KV ? wait_a(it + 1) : wait_b(it + 1))) break;
+            for (int it = 0; it < tk.n && ok; ++it) {
+                if (!(ok = warp_wait(&bars.p_full[it & 1], (it >> 1) & 1u, bars.abort_flag, a.timeout_ns))) break;
+                tc_fence_after();
                 if (elect_one_sync()) {
-                    issue_dp(it + 1);
-                    if (!KV) {
-                        mma_commit(bars.s_full);
+                    issue_acc(it);
+                    mma_commit(&bars.empty_a[it % L::kSA]);
+                }
+                __syncwarp();
+                if (it + 2 < tk.n) {  // tile it+2 into the buffer tile it has just released
+                    if (!(ok = wait_a(it + 2))) break;
+                    if (elect_one_sync()) {
+                        issue_s(it + 2);
+                        issue_dp(it + 2);
+                        mma_commit(&bars.s_full[it & 1]);
+                    }
+                    __syncwarp();
+                }
+            }
+        } else {
+            if (ok && (ok = wait_a(0) && wait_b(0))) {
+                if (elect_one_sync()) {
+                    issue_s(0);
+                    issue_dp(0);
+                    mma_commit(&bars.s_full[0]);
+                    mma_commit(&bars.empty_b[0]);
+                }
+                __syncwarp();
+            }
+            for (int it = 0; it < tk.n && ok; ++it) {
+                const bool more = it + 1 < tk.n;
+                if (more) {
+                    if (!(ok = wait_a(it + 1))) break;
+                    if (elect_one_sync()) issue_s(it + 1);
+                    __syncwarp();
+                }
+                if (!(ok = warp_wait(bars.dp_free, it & 1u, bars.abort_flag, a.timeout_ns))) break;
+                tc_fence_after();
+                if (more) {
+                    if (!(ok = wait_b(it + 1))) break;
+                    if (elect_one_sync()) {
+                        issue_dp(it + 1);
+                        mma_commit(&bars.s_full[(it + 1) & 1]);
                         mma_commit(&bars.empty_b[(it + 1) % L::kSBm]);  // V slot free once dP is done
                     }
+                    __syncwarp();
+                }
+                if (!(ok = warp_wait(&bars.p_full[it & 1], (it >> 1) & 1u, bars.abort_flag, a.timeout_ns))) break;
+                tc_fence_after();
+                if (elect_one_sync()) {
+                    issue_acc(it);
+                    mma_commit(&bars.empty_a[it % L::kSA]);
                 }
                 __syncwarp();
             }
-            if (!(ok = warp_wait(bars.p_full, it & 1u, bars.abort_flag, a.timeout_ns))) break;
-            tc_fence_after();
-            if (elect_one_sync()) {
-                issue_acc(it);
-                mma_commit(&bars.empty_a[it % L::kSA]);
-                if (KV && more) {
-                    issue_s(it + 1);
-                    mma_commit(bars.s_full);
-                }
-            }
-            __syncwarp();
         }
         if (elect_one_sync()) mma_commit(bars.done);  // fires once every MMA above has completed
         __syncwarp();
     } else {
         // ---------------- elementwise warps 0-7 ----------------
         // Warps w and w+4 share TMEM lane quarter w % 4 (thread = lane =
-        // resident row); warp w < 4 takes columns [0,64) of S and dP, warp
-        // w + 4 columns [64,128), and each writes its 16-bit results into the
-        // S columns it has already read.
+        // resident row) and split the columns of S and dP between them (dK/dV:
+        // 32 each of a 64-query tile; dQ: 64 each of a 128-key tile); each
+        // writes its 16-bit results into the S columns it has already read.
         const int quarter = warp % 4, half = warp / 4;
         const int r = quarter * 32 + lane;
         const int row = blk0 + r;  // KV: key index; dQ: query index
@@ -405,18 +443,61 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             delta_r = stats[a.Npad];
         }
         bool ok = true;
-        for (int it = 0; it < tk.n && ok; ++it) {
+        if (KV) {
+            // 64-query tile it: this warp's 32 columns [32*half, 32*half+32)
+            // of S^T and dP^T in buffer it & 1; P^T and dS^T go to the first
+            // 16 and the next 16 of those S^T columns.
+            for (int it = 0; it < tk.n && ok; ++it) {
+                const int jq = tk.j0 + it;  // 64-query tile index
+                const int sa = it % L::kSA;
+                ok = warp_wait(&bars.s_full[it & 1], (it >> 1) & 1u, bars.abort_flag, a.timeout_ns);
+                if (ok)  // the slot's statistics: this phase is complete and not yet refilled
+                    ok = warp_wait(&bars.full_a[sa], (it / L::kSA) & 1u, bars.abort_flag, a.timeout_ns);
+                if (!ok) break;
+                tc_fence_after();
+                const float* lse2s = reinterpret_cast<const float*>(smem + L::kRingA + sa * L::kSlotA +
+                                                                    2 * L::kTileIn);
+                const float* deltas = lse2s + kBQ;
+                // queries before this key row exist only in the tiles that meet the block's diagonal
+                const bool diag = CAUSAL && jq < 2 * tk.blk + 2;
+                const int qoff = jq * kBQ - blk0;  // query - key = qoff + col - r
+                const uint32_t sb = t_s + 128u * static_cast<uint32_t>(it & 1) + lane_off + 32u * half;
+                uint32_t sv[32], dpv[32];
+                tmem_ld32(sb, sv);
+                tmem_ld32(sb + 64, dpv);
+                tmem_wait_ld();
+                reg_fence(sv);
+                reg_fence(dpv);
+                uint32_t pk[16], dsk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float p[2], ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int col = 32 * half + e + u;  // query jq*64 + col
+                        float pv = ex2_approx(__uint_as_float(sv[e + u]) * a.sl2 - lse2s[col]);
+                        if (diag && qoff + col < r) pv = 0.f;
+                        p[u] = pv;
+                        ds[u] = pv * (__uint_as_float(dpv[e + u]) - deltas[col]);
+                    }
+                    pk[e / 2] = pack16(p[0], p[1], BF16);
+                    dsk[e / 2] = pack16(ds[0], ds[1], BF16);
+                }
+                tmem_st16(sb, pk);
+                tmem_st16(sb + 16, dsk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.p_full[it & 1]);
+            }
+        }
+        for (int it = 0; !KV && it < tk.n && ok; ++it) {
             const int j = tk.j0 + it;
-            const int s = it % L::kSA;
-            ok = warp_wait(bars.s_full, it & 1u, bars.abort_flag, a.timeout_ns);
-            if (KV && ok)  // the stage's statistics: this phase is complete and not yet refilled
-                ok = warp_wait(&bars.full_a[s], (it / L::kSA) & 1u, bars.abort_flag, a.timeout_ns);
+            ok = warp_wait(&bars.s_full[it & 1], (it >> 1) & 1u, bars.abort_flag, a.timeout_ns);
             if (!ok) break;
             tc_fence_after();
-            const float* lse2s = reinterpret_cast<const float*>(smem + L::kRingA + s * L::kSlotA + 2 * L::kTile);
-            const float* deltas = lse2s + kBT;
             const bool diag = CAUSAL && j == tk.blk;
-            const uint32_t sb = (KV ? t_s : t_s + 128u * static_cast<uint32_t>(it & 1)) + lane_off + c0;
+            const uint32_t sb = t_s + 128u * static_cast<uint32_t>(it & 1) + lane_off + c0;
             // dP first, in full, so that its columns can be handed back at once.
             uint32_t dpv[2][32], sv[32];
             tmem_ld32(t_dp + lane_off + c0, dpv[0]);
@@ -436,40 +517,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                     tmem_wait_ld();
                     reg_fence(sv);
                 }
-                uint32_t pk[16], dsk[16];
+                uint32_t dsk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    float p[2], ds[2];
+                    float ds[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const int col = c0 + c * 32 + e + u;  // KV: query j*128+col; dQ: key j*128+col
-                        const float lse2 = KV ? lse2s[col] : lse2_r;
-                        const float dlt = KV ? deltas[col] : delta_r;
-                        float pv = ex2_approx(__uint_as_float(sv[e + u]) * a.sl2 - lse2);
-                        if (KV) {
-                            if (diag && col < r) pv = 0.f;  // query j*128+col before key row
-                        } else {
-                            const int key = j * kBT + col;
-                            if (key >= a.N || (diag && col > r)) pv = 0.f;
-                        }
-                        p[u] = pv;
-                        ds[u] = pv * (__uint_as_float(dpv[c][e + u]) - dlt);
+                        const int col = c0 + c * 32 + e + u;  // key j*128+col
+                        float pv = ex2_approx(__uint_as_float(sv[e + u]) * a.sl2 - lse2_r);
+                        const int key = j * kBT + col;
+                        if (key >= a.N || (diag && col > r)) pv = 0.f;
+                        ds[u] = pv * (__uint_as_float(dpv[c][e + u]) - delta_r);
                     }
-                    pk[e / 2] = pack16(p[0], p[1], BF16);
                     dsk[e / 2] = pack16(ds[0], ds[1], BF16);
                 }
                 // Only columns of this chunk, already read, are overwritten.
-                if (KV) {
-                    tmem_st16(sb + c * 32, pk);
-                    tmem_st16(sb + c * 32 + 16, dsk);
-                } else {
-                    tmem_st16(sb + c * 32, dsk);
-                }
+                tmem_st16(sb + c * 32, dsk);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.p_full);
+            if (lane == 0) mbar_arrive(&bars.p_full[it & 1]);
         }
         // ---------------- epilogue: accumulators -> 16-bit rows ----------------
         // Each warp converts half of the D columns of its 32 rows.
