@@ -55,6 +55,8 @@ class OracleLib:
                                              ctypes.c_double, ci, i64p, i64p, i64, dp, dp, ci]
         lib.attn_oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64,
                                         ctypes.c_double, ci, ci]
+        lib.attn_oracle_bwd_gqa.argtypes = [dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64, i64,
+                                            ctypes.c_double, ci, ci]
         lib.attn_oracle_bwd_stats.argtypes = [dp, dp, dp, dp, i64, i64, i64, i64,
                                               ctypes.c_double, ci, i64p, i64, dp, dp, ci]
         lib.attn_oracle_bwd_dq_rows.argtypes = [dp, dp, dp, dp, i64, i64, i64, i64,
@@ -66,7 +68,7 @@ class OracleLib:
         lib.attn_oracle_default_threads.argtypes = []
         for f in ("attn_oracle_fwd", "attn_oracle_rows", "attn_oracle_probs",
                   "attn_oracle_online_fwd", "attn_oracle_fwd_gqa", "attn_oracle_rows_gqa",
-                  "attn_oracle_bwd", "attn_oracle_bwd_stats", "attn_oracle_bwd_dq_rows",
+                  "attn_oracle_bwd", "attn_oracle_bwd_gqa", "attn_oracle_bwd_stats", "attn_oracle_bwd_dq_rows",
                   "attn_oracle_bwd_dkdv_rows", "attn_oracle_default_threads"):
             getattr(lib, f).restype = ci
         self._lib = lib
@@ -184,6 +186,24 @@ class OracleLib:
             raise RuntimeError("attn_oracle_bwd failed: %d" % rc)
         return dq, dk, dv
 
+    def backward_gqa(self, q, k, v, dout, scale, causal=False, nthreads=0):
+        """Grouped-query backward: q, dout [B,H,N,D]; k, v [B,Hkv,N,D].
+        Returns (dq [B,H,N,D], dk, dv [B,Hkv,N,D]) fp64."""
+        q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
+        B, H, N, D = q.shape
+        Hkv = k.shape[1]
+        if k.shape != (B, Hkv, N, D) or v.shape != k.shape or do.shape != q.shape:
+            raise ValueError("q, dout [B,H,N,D]; k, v [B,Hkv,N,D]")
+        dq = np.full((B, H, N, D), np.nan, np.float64)
+        dk = np.full((B, Hkv, N, D), np.nan, np.float64)
+        dv = np.full((B, Hkv, N, D), np.nan, np.float64)
+        rc = self._lib.attn_oracle_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk),
+                                           _ptr(dv), B, H, Hkv, N, D, float(scale),
+                                           int(bool(causal)), int(nthreads))
+        if rc != 0:
+            raise RuntimeError("attn_oracle_bwd_gqa failed: %d" % rc)
+        return dq, dk, dv
+
     def backward_rows(self, q, k, v, dout, scale, causal, bh_rows, rows, bh_keys, keys,
                       nthreads=0):
         """Selected rows of dQ (heads bh_rows, query rows `rows`) and of dK, dV
@@ -268,6 +288,10 @@ def backward(q, k, v, dout, scale, causal=False, nthreads=0):
     return _get().backward(q, k, v, dout, scale, causal, nthreads)
 
 
+def backward_gqa(q, k, v, dout, scale, causal=False, nthreads=0):
+    return _get().backward_gqa(q, k, v, dout, scale, causal, nthreads)
+
+
 def backward_rows(q, k, v, dout, scale, causal, bh_rows, rows, bh_keys, keys, nthreads=0):
     return _get().backward_rows(q, k, v, dout, scale, causal, bh_rows, rows, bh_keys, keys,
                                 nthreads)
@@ -278,6 +302,6 @@ def lib_path() -> str:
 
 
 __all__ = ["OracleLib", "attention", "attention_rows", "probabilities",
-           "attention_online", "attention_gqa", "attention_rows_gqa", "backward",
+           "attention_online", "attention_gqa", "attention_rows_gqa", "backward", "backward_gqa",
            "backward_rows", "default_threads",
            "lib_path"]

@@ -688,3 +688,88 @@ int attn_oracle_bwd(const double* q, const double* k, const double* v, const dou
     free(heads); free(slot); free(idx); free(lse); free(delta);
     return rc;
 }
+
+/* ---------------------------------------------------------------------------
+ * Backward of grouped-query attention: query head h of batch b reads key/value
+ * head b*Hkv + h/(H/Hkv), so by the chain rule the gradient of a shared key or
+ * value row is the sum of the per-query-head gradients over the H/Hkv query
+ * heads that read it; dQ is per query head as before.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    const double *q, *k, *v, *dout;
+    int64_t H, Hkv, N, D;
+    double scale;
+    int causal;
+    double *lse, *delta;   /* [B*H][N] */
+    double *dq, *dk, *dv;  /* dq [B,H,N,D]; dk, dv [B,Hkv,N,D] */
+} gqa_bwd_ctx;
+
+static int64_t gqa_kv_head(const gqa_bwd_ctx* c, int64_t bh)
+{
+    const int64_t b = bh / c->H, h = bh % c->H;
+    return b * c->Hkv + h / (c->H / c->Hkv);
+}
+
+static void gqa_stats_item(const void* vctx, int64_t it, double* s)
+{
+    const gqa_bwd_ctx* c = (const gqa_bwd_ctx*)vctx;
+    const int64_t bh = it / c->N, i = it % c->N;
+    const int64_t qo = bh * c->N * c->D, ko = gqa_kv_head(c, bh) * c->N * c->D;
+    bwd_row_stats(c->q + qo, c->k + ko, c->v + ko, c->dout + qo, c->N, c->D, c->scale, c->causal,
+                  i, s, c->lse + it, c->delta + it);
+}
+
+static void gqa_dq_item(const void* vctx, int64_t it, double* s)
+{
+    const gqa_bwd_ctx* c = (const gqa_bwd_ctx*)vctx;
+    (void)s;
+    const int64_t bh = it / c->N, i = it % c->N;
+    const int64_t qo = bh * c->N * c->D, ko = gqa_kv_head(c, bh) * c->N * c->D;
+    bwd_dq_row(c->q + qo, c->k + ko, c->v + ko, c->dout + qo, c->N, c->D, c->scale, c->causal, i,
+               c->lse[it], c->delta[it], c->dq + it * c->D);
+}
+
+/* item = (kv head, key j): sum over the query heads of the group; scratch
+ * holds one dK row and one dV row of a single query head. */
+static void gqa_dkdv_item(const void* vctx, int64_t it, double* s)
+{
+    const gqa_bwd_ctx* c = (const gqa_bwd_ctx*)vctx;
+    const int64_t kvh = it / c->N, j = it % c->N;
+    const int64_t b = kvh / c->Hkv, hk = kvh % c->Hkv, G = c->H / c->Hkv;
+    const int64_t ko = kvh * c->N * c->D;
+    double* dk_row = c->dk + it * c->D;
+    double* dv_row = c->dv + it * c->D;
+    for (int64_t d = 0; d < c->D; ++d) { dk_row[d] = 0.0; dv_row[d] = 0.0; }
+    for (int64_t g = 0; g < G; ++g) {
+        const int64_t bh = b * c->H + hk * G + g;
+        const int64_t qo = bh * c->N * c->D;
+        bwd_dkdv_row(c->q + qo, c->k + ko, c->v + ko, c->dout + qo, c->N, c->D, c->scale, c->causal,
+                     j, c->lse + bh * c->N, c->delta + bh * c->N, s, s + c->D);
+        for (int64_t d = 0; d < c->D; ++d) { dk_row[d] += s[d]; dv_row[d] += s[c->D + d]; }
+    }
+}
+
+int attn_oracle_bwd_gqa(const double* q, const double* k, const double* v, const double* dout,
+                        double* dq, double* dk, double* dv,
+                        int64_t B, int64_t H, int64_t Hkv, int64_t N, int64_t D,
+                        double scale, int causal, int nthreads)
+{
+    if (check_shape(B, H, N, D) || check_heads(H, Hkv)) return -1;
+    if (B * H * N == 0) return 0;
+    if (!q || !k || !v || !dout || !dq || !dk || !dv) return -2;
+    double* lse = (double*)malloc(sizeof(double) * (size_t)(B * H * N));
+    double* delta = (double*)malloc(sizeof(double) * (size_t)(B * H * N));
+    int rc = -3;
+    if (lse && delta) {
+        gqa_bwd_ctx c;
+        memset(&c, 0, sizeof(c));
+        c.q = q; c.k = k; c.v = v; c.dout = dout;
+        c.H = H; c.Hkv = Hkv; c.N = N; c.D = D; c.scale = scale; c.causal = causal;
+        c.lse = lse; c.delta = delta; c.dq = dq; c.dk = dk; c.dv = dv;
+        rc = parallel_items(gqa_stats_item, &c, B * H * N, N, nthreads);
+        if (rc == 0) rc = parallel_items(gqa_dq_item, &c, B * H * N, 1, nthreads);
+        if (rc == 0) rc = parallel_items(gqa_dkdv_item, &c, B * Hkv * N, 2 * D, nthreads);
+    }
+    free(lse); free(delta);
+    return rc;
+}

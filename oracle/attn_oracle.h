@@ -133,6 +133,14 @@ int attn_oracle_bwd_dkdv_rows(const double* q, const double* k, const double* v,
                               const int64_t* slot_idx, const int64_t* key_idx, int64_t nkeys,
                               double* dk_rows, double* dv_rows, int nthreads);
 
+/* Backward of grouped-query attention (k, v, dk, dv are [B,Hkv,N,D]): dQ per
+ * query head; the dK and dV rows of a shared key/value head are the sums of
+ * the per-query-head gradients over the H/Hkv query heads that read it. */
+int attn_oracle_bwd_gqa(const double* q, const double* k, const double* v, const double* dout,
+                        double* dq, double* dk, double* dv,
+                        int64_t B, int64_t H, int64_t Hkv, int64_t N, int64_t D,
+                        double scale, int causal, int nthreads);
+
 /* Number of threads nthreads<=0 resolves to (CPUs in the affinity mask). */
 int attn_oracle_default_threads(void);
 

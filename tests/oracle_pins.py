@@ -370,9 +370,48 @@ def pin_bwd_rows_match_full(orc):
         _close(sv, dv.reshape(B * H, N, D)[bh_k, keys], 0.0, "rows dV")
 
 
+def pin_bwd_gqa(orc):
+    """Grouped-query backward: Hkv = H is the multi-head backward; otherwise
+    dQ equals the multi-head dQ on K/V repeated per group, and the dK, dV of a
+    shared head equal the sums of the repeated heads' gradients over the
+    group; and on a tiny case, the gradient of a shared key equals central
+    differences of the grouped-query forward."""
+    r = _rng(45)
+    B, H, N, D = 2, 6, 11, 4
+    q = r.standard_normal((B, H, N, D))
+    do = r.standard_normal((B, H, N, D))
+    for Hkv in (1, 2, 3, 6):
+        k = r.standard_normal((B, Hkv, N, D))
+        v = r.standard_normal((B, Hkv, N, D))
+        G = H // Hkv
+        for causal in (False, True):
+            dq, dk, dv = orc.backward_gqa(q, k, v, do, 0.7, causal)
+            rq, rk, rv = orc.backward(q, np.repeat(k, G, axis=1), np.repeat(v, G, axis=1), do, 0.7, causal)
+            _close(dq, rq, 1e-12, "gqa dQ Hkv=%d" % Hkv)
+            _close(dk, rk.reshape(B, Hkv, G, N, D).sum(axis=2), 1e-12, "gqa dK Hkv=%d" % Hkv)
+            _close(dv, rv.reshape(B, Hkv, G, N, D).sum(axis=2), 1e-12, "gqa dV Hkv=%d" % Hkv)
+    q, do = r.standard_normal((1, 4, 5, 3)), r.standard_normal((1, 4, 5, 3))
+    k, v = r.standard_normal((1, 2, 5, 3)), r.standard_normal((1, 2, 5, 3))
+    for causal in (False, True):
+        _, dk, dv = orc.backward_gqa(q, k, v, do, 0.8, causal)
+        h = 1e-6
+        for t, (x, g) in enumerate(((k, dk), (v, dv))):
+            for idx in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args_p = [k, v]
+                args_m = [k, v]
+                args_p[t], args_m[t] = xp, xm
+                lp = float(np.sum(orc.attention_gqa(q, *args_p, 0.8, causal)[0] * do))
+                lm = float(np.sum(orc.attention_gqa(q, *args_m, 0.8, causal)[0] * do))
+                fd = (lp - lm) / (2 * h)
+                assert abs(fd - g[idx]) <= 1e-7 * (1 + abs(fd)), ("gqa finite differences", t, idx, fd, g[idx])
+
+
 ALL_PINS = [pin_row_sums, pin_ones_v, pin_zero_q, pin_basis_v, pin_shift_invariance,
             pin_single_key, pin_causal_first_rows, pin_permutation, pin_bruteforce,
             pin_rows_match_full, pin_online_matches_definition, pin_golden_dot,
             pin_golden_max_row, pin_gqa_equals_repeated_heads, pin_gqa_bruteforce,
             pin_bwd_finite_differences, pin_bwd_closed_forms, pin_bwd_invariances,
-            pin_bwd_rows_match_full]
+            pin_bwd_rows_match_full, pin_bwd_gqa]

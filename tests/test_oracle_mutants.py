@@ -60,6 +60,10 @@ MUTANTS = [
      "int64_t nvis = N;\n    if (nvis > N) nvis = N;\n    for (int64_t c = 0; c < D; ++c) dq_row[c] = 0.0;"),
     ("bwd_dp_wrong_row", "for (int64_t c = 0; c < D; ++c) dp += doi[c] * vj[c];\n        const double p = exp(scale * dot - lse_i);",
      "for (int64_t c = 0; c < D; ++c) dp += doh[c] * vj[c];\n        const double p = exp(scale * dot - lse_i);"),
+    ("bwd_gqa_first_head_only", "for (int64_t g = 0; g < G; ++g) {\n        const int64_t bh = b * c->H + hk * G + g;",
+     "for (int64_t g = 0; g < 1; ++g) {\n        const int64_t bh = b * c->H + hk * G + g;"),
+    ("bwd_gqa_interleaved_heads", "const int64_t bh = b * c->H + hk * G + g;", "const int64_t bh = b * c->H + g * c->Hkv + hk;"),
+    ("bwd_gqa_kv_head_mod", "return b * c->Hkv + h / (c->H / c->Hkv);", "return b * c->Hkv + h % c->Hkv;"),
     ("gqa_no_batch_offset", "const int64_t kvh = b * jb->Hkv + h / (jb->H / jb->Hkv);",
      "const int64_t kvh = h / (jb->H / jb->Hkv) + 0 * b;"),
 ]
