@@ -156,7 +156,8 @@ FATTN_API int64_t fattn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N);
  *                      fattn_bwd_workspace_bytes(B, H, N) bytes, 16-byte
  *                      aligned, overlapping nothing else; contents ignored.
  *   dtype            : FATTN_BF16 or FATTN_F16 (FATTN_F32 -> FATTN_ERR_UNSUPPORTED).
- *   B,H,N,D,scale,causal : as fattn_fwd (multi-head: k and v have q's shape).
+ *   B,H,N,D,scale,causal : as fattn_fwd (multi-head: k and v have q's shape;
+ *                      fattn_bwd_gqa below takes shared K/V heads).
  *
  * Three kernel launches on `stream` (row statistics, dK/dV, dQ); each
  * gradient row is produced by exactly one CTA, so the result is
@@ -166,6 +167,24 @@ FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, const void*
               const void* dout, const float* lse, void* dq, void* dk, void* dv,
               void* workspace, int64_t workspace_bytes, int64_t B, int64_t H, int64_t N,
               int64_t D, float scale, int causal, int dtype, fattn_stream_t stream);
+
+/*
+ * fattn_bwd_gqa -- the backward of grouped-query / multi-query attention
+ * (the forward is fattn_fwd_gqa): k, v, dk and dv are [B, Hkv, N, D] with H a
+ * multiple of Hkv, query head h of batch b reads key/value head
+ * b*Hkv + h/(H/Hkv), and the dK and dV rows of a shared head are the sums of
+ * the gradients of the H/Hkv query heads that read it (the chain rule through
+ * the shared rows).  q, o, dout, dq are [B, H, N, D], lse [B, H, N]; the
+ * workspace is sized by fattn_bwd_workspace_bytes(B, H, N).  Each dK/dV
+ * row is still produced by one CTA, which loops over the group's query
+ * heads: no atomics, deterministic.  Hkv == H is fattn_bwd.  Other rules
+ * and errors as fattn_bwd.
+ */
+FATTN_API int fattn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                  const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                  void* workspace, int64_t workspace_bytes, int64_t B, int64_t H, int64_t Hkv,
+                  int64_t N, int64_t D, float scale, int causal, int dtype,
+                  fattn_stream_t stream);
 
 /*
  * fattn_unfused_workspace_bytes -- bytes of device workspace fattn_fwd_unfused

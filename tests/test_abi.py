@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
     for name in ("fattn_fwd", "fattn_fwd_gqa", "fattn_fwd_host", "fattn_plan",
                  "fattn_get_device_status", "fattn_selftest_wait_timeout",
                  "fattn_fwd_unfused", "fattn_unfused_workspace_bytes",
-                 "fattn_bwd", "fattn_bwd_workspace_bytes",
+                 "fattn_bwd", "fattn_bwd_gqa", "fattn_bwd_workspace_bytes",
                  "fattn_status_string", "fattn_version"):
         assert name in syms
 
@@ -134,6 +134,13 @@ def test_bwd_workspace_and_argument_errors(lib):
     assert bwd(dv=4 * T) == INVALID          # dV over O
     assert bwd(ws=2 * T) == INVALID          # workspace over K
     assert bwd(B=0) == OK
+
+    def bwd_gqa(Hkv, H=4, dk=8 * T, **kw):
+        return lib.fattn_bwd_gqa(T, 2 * T, 3 * T, 4 * T, 5 * T, 6 * T, 7 * T, dk, 9 * T, 10 * T,
+                                 1 << 30, 1, H, Hkv, 16, 64, 0.125, 0, 2, None)
+    assert bwd_gqa(Hkv=3) == INVALID       # 4 % 3 != 0
+    assert bwd_gqa(Hkv=0) == INVALID
+    assert bwd_gqa(Hkv=8) == INVALID       # more K/V heads than query heads
 
 
 def test_unfused_argument_errors(lib):

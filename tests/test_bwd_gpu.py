@@ -131,3 +131,69 @@ def test_bwd_full_size_sampled(w):
         check_head(q64[0, 0], k64[0, 0], v64[0, 0], do64[0, 0], o_ref[0, 0], lse_ref[0, 0], gh,
                    w.scale, w.causal, w.torch_dtype, idx, idx, "bwd %s head %d" % (w.name, bh),
                    dq_ref, dk_ref, dv_ref)
+
+
+def make_gqa(B, H, Hkv, N, D, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, H, N, D, generator=g).to(dtype)
+    k = torch.randn(B, Hkv, N, D, generator=g).to(dtype)
+    v = torch.randn(B, Hkv, N, D, generator=g).to(dtype)
+    do = torch.randn(B, H, N, D, generator=g).to(dtype)
+    return q, k, v, do
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("fp16", 64)])
+@pytest.mark.parametrize("Hkv", [1, 2])
+def test_bwd_gqa_matches_oracle(Hkv, dtype, D, causal):
+    """Grouped-query backward: dQ per query head and dK, dV summed over each
+    group, against the oracle's grouped-query backward; the bound of a shared
+    row is the sum of the per-query-head bounds plus one output rounding."""
+    B, H, N = 1, 4, 300
+    dt = DT[dtype]
+    q, k, v, do = make_gqa(B, H, Hkv, N, D, dt, 60 + Hkv + D)
+    scale = fattn._default_scale(D)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fattn.fwd(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = fattn.bwd(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fattn.get_device_status() == 0
+    assert dk.shape == k.shape and dv.shape == v.shape and dq.shape == q.shape
+    q64, k64, v64, do64 = (to_f64(t) for t in (q, k, v, do))
+    dq_ref, dk_ref, dv_ref = oracle.backward_gqa(q64, k64, v64, do64, scale, causal)
+    o_ref, lse_ref = oracle.attention_gqa(q64, k64, v64, scale, causal)
+    G = H // Hkv
+    allr = np.arange(N)
+    gq, gk, gv = to_f64(dq), to_f64(dk), to_f64(dv)
+    for hk in range(Hkv):
+        bk = np.zeros((N, D))
+        bv = np.zeros((N, D))
+        for g in range(G):
+            h = hk * G + g
+            bq = bwd_bound_dq(q64[0, h], k64[0, hk], v64[0, hk], do64[0, h], o_ref[0, h], lse_ref[0, h],
+                              scale, causal, allr, dt, dq_ref[0, h])
+            compare_bound(gq[0, h], dq_ref[0, h], bq, "gqa dQ head %d" % h)
+            zk, zv = bwd_bound_dkdv(q64[0, h], k64[0, hk], v64[0, hk], do64[0, h], o_ref[0, h],
+                                    lse_ref[0, h], scale, causal, allr, dt, np.zeros((N, D)),
+                                    np.zeros((N, D)))
+            bk += zk
+            bv += zv
+        from tests.parity import half_ulp
+        compare_bound(gk[0, hk], dk_ref[0, hk], bk + half_ulp(dk_ref[0, hk], dt), "gqa dK head %d" % hk)
+        compare_bound(gv[0, hk], dv_ref[0, hk], bv + half_ulp(dv_ref[0, hk], dt), "gqa dV head %d" % hk)
+
+
+def test_bwd_gqa_dq_equals_mha_on_repeated_heads():
+    """dQ of a query head depends on its K/V head only, so the grouped-query
+    dQ is bit-identical to the multi-head dQ on explicitly repeated K/V."""
+    B, H, Hkv, N, D = 1, 8, 2, 400, 128
+    q, k, v, do = make_gqa(B, H, Hkv, N, D, torch.bfloat16, 3)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fattn.fwd(qd, kd, vd, causal=True)
+    dq1, _, _ = fattn.bwd(qd, kd, vd, o, lse, dod, causal=True)
+    kr = kd.repeat_interleave(H // Hkv, dim=1).contiguous()
+    vr = vd.repeat_interleave(H // Hkv, dim=1).contiguous()
+    dq2, _, _ = fattn.bwd(qd, kr, vr, o, lse, dod, causal=True)
+    torch.cuda.synchronize()
+    assert fattn.get_device_status() == 0
+    assert torch.equal(dq1, dq2)

@@ -71,6 +71,8 @@ def load():
                                       ci, vp]
     lib.fattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, f32,
                               ci, ci, vp]
+    lib.fattn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                  i64, f32, ci, ci, vp]
     lib.fattn_bwd_workspace_bytes.argtypes = [i64, i64, i64]
     lib.fattn_bwd_workspace_bytes.restype = i64
     lib.fattn_fwd_unfused_static.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, ci, ci, vp]
@@ -82,7 +84,7 @@ def load():
     lib.fattn_status_string.argtypes = [ci]
     lib.fattn_status_string.restype = ctypes.c_char_p
     lib.fattn_version.argtypes = []
-    for f in ("fattn_fwd", "fattn_fwd_gqa", "fattn_fwd_host", "fattn_fwd_unfused", "fattn_bwd",
+    for f in ("fattn_fwd", "fattn_fwd_gqa", "fattn_fwd_host", "fattn_fwd_unfused", "fattn_bwd", "fattn_bwd_gqa",
               "fattn_fwd_unfused_static", "fattn_plan", "fattn_get_device_status",
               "fattn_selftest_wait_timeout", "fattn_version"):
         getattr(lib, f).restype = ci
@@ -197,12 +199,13 @@ def bwd_workspace_bytes(B, H, N):
 def bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None, dv=None,
         workspace=None, stream=None):
     """Attention backward on CUDA tensors: gradients of sum(dout * O) where
-    (o, lse) is what ``fwd`` returned for (q, k, v).  bfloat16 / float16,
-    q, k, v, o, dout of one [B, H, N, D] shape, lse float32 [B, H, N].
-    Returns (dq, dk, dv) in the input dtype.  ``workspace`` (a CUDA uint8
-    tensor of at least ``bwd_workspace_bytes(B, H, N)`` bytes) is allocated
-    here when None."""
-    _check_qkv(q, k, v)
+    (o, lse) is what ``fwd`` returned for (q, k, v).  bfloat16 / float16;
+    q, o, dout [B, H, N, D]; k, v [B, Hkv, N, D] with H a multiple of Hkv
+    (grouped-query attention when Hkv < H: dk, dv are summed over each
+    group); lse float32 [B, H, N].  Returns (dq, dk, dv) in the input dtype
+    with q's and k's shapes.  ``workspace`` (a CUDA uint8 tensor of at least
+    ``bwd_workspace_bytes(B, H, N)`` bytes) is allocated here when None."""
+    _check_qkv(q, k, v, allow_gqa=True)
     for t in (o, dout):
         if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
             raise ValueError("o and dout must be contiguous with q's shape and dtype")
@@ -211,22 +214,24 @@ def bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None, dv=No
     if not q.is_cuda:
         raise ValueError("bwd needs CUDA tensors")
     B, H, N, D = q.shape
+    Hkv = k.shape[1]
     if scale is None:
         scale = _default_scale(D)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
     if workspace is None:
         workspace = torch.empty(max(bwd_workspace_bytes(B, H, N), 16), dtype=torch.uint8,
                                 device=q.device)
     lib = load()
     with torch.cuda.device(q.device):
-        rc = lib.fattn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
-                           lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                           workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                           B, H, N, D, float(scale), int(bool(causal)), DTYPE_CODES[q.dtype],
-                           _stream_handle(stream))
-    _check(rc, "fattn_bwd")
+        rc = lib.fattn_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                               dv.data_ptr(), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), B, H, Hkv, N, D,
+                               float(scale), int(bool(causal)), DTYPE_CODES[q.dtype],
+                               _stream_handle(stream))
+    _check(rc, "fattn_bwd_gqa")
     return dq, dk, dv
 
 

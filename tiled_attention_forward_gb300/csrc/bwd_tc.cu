@@ -131,22 +131,26 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
                                                      timeout_ns));
 }
 
-// Work unit of a CTA.  dKdV: key block kb of head bh, 64-query tiles
-// j0 .. 2*nt-1 (causal: from the first tile that meets the block's diagonal).  dQ: query tile qt of head bh, key
-// tiles 0 .. j_end-1 (causal: up to the diagonal).  Causal grids run the
-// longest units first (ascending kb, descending qt); otherwise head-major.
+// Work unit of a CTA.  dKdV: key block kb of key/value head bh (B*Hkv of
+// them); the inner tiles are the 64-query tiles j0 .. 2*nt-1 (causal: from the
+// first tile that meets the block's diagonal) of each of the H/Hkv query heads
+// that read this K/V head, head after head (n = group size x tiles per head).
+// dQ: query tile qt of query head bh, key tiles 0 .. j_end-1 (causal: up to
+// the diagonal) of its K/V head.  Causal grids run the longest units first
+// (ascending kb, descending qt); otherwise head-major.
 struct BwdTask {
-    int bh, blk, j0, n;
+    int bh, blk, j0, n, per_head;
 };
 
 template <bool KV, bool CAUSAL>
 __device__ __forceinline__ BwdTask bwd_task(const BwdArgs& a) {
     BwdTask t;
     const int idx = blockIdx.x;
+    const int heads = KV ? a.BHkv : a.BH;
     if (CAUSAL) {
         // longest first: across heads, by block
-        t.bh = idx % a.BH;
-        t.blk = KV ? idx / a.BH : a.num_tiles - 1 - idx / a.BH;
+        t.bh = idx % heads;
+        t.blk = KV ? idx / heads : a.num_tiles - 1 - idx / heads;
     } else {
         // head-major: CTAs running together stream the same head's tiles (L2 reuse)
         t.bh = idx / a.num_tiles;
@@ -154,12 +158,21 @@ __device__ __forceinline__ BwdTask bwd_task(const BwdArgs& a) {
     }
     if (KV) {  // 64-query inner tiles: two per 128-key block
         t.j0 = CAUSAL ? 2 * t.blk : 0;
-        t.n = 2 * a.num_tiles - t.j0;
+        t.per_head = 2 * a.num_tiles - t.j0;
+        t.n = t.per_head * (a.H / a.Hkv);
     } else {
         t.j0 = 0;
-        t.n = CAUSAL ? t.blk + 1 : a.num_tiles;
+        t.per_head = CAUSAL ? t.blk + 1 : a.num_tiles;
+        t.n = t.per_head;
     }
     return t;
+}
+
+// Query head read by inner tile it of a dK/dV task: the group's query heads
+// one after the other.
+__device__ __forceinline__ int bwd_query_head(const BwdArgs& a, const BwdTask& tk, int it) {
+    const int b = tk.bh / a.Hkv, hk = tk.bh % a.Hkv, G = a.H / a.Hkv;
+    return b * a.H + hk * G + it / tk.per_head;
 }
 
 template <int D, bool BF16, bool KV, bool CAUSAL>
@@ -212,7 +225,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
     const uint32_t t_acc1 = KV ? tmem + 256 : tmem + 384;
     const uint32_t t_acc2 = tmem + 256 + D;
     const int blk0 = tk.blk * kBT;  // first row of the resident tiles
-    const int kvh = tk.bh;          // multi-head: K/V head = query head
+    // K/V head of the task (dK/dV: the task's own head; dQ: the one its query head reads)
+    const int kvh = KV ? tk.bh : kv_head_of(tk.bh, a.H, a.Hkv);
 
     if (warp == kTmaWarp) {
         // ---------------- TMA producer ----------------
@@ -222,15 +236,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             const CUtensorMap* inner1 = KV ? &a.tmap_q64 : &a.tmap_k;
             const CUtensorMap* inner2 = KV ? &a.tmap_do64 : &a.tmap_v;
             mbar_arrive_expect_tx(bars.outer_full, 2 * L::kTile);
+            const int oh = KV ? kvh : tk.bh;  // head of the resident tiles
             for (int at = 0; at < D / 64; ++at) {
-                tma_load_3d(smem + L::kOuter + at * kBT * 128, outer1, bars.outer_full, at * 64, blk0, kvh);
+                tma_load_3d(smem + L::kOuter + at * kBT * 128, outer1, bars.outer_full, at * 64, blk0, oh);
                 tma_load_3d(smem + L::kOuter + L::kTile + at * kBT * 128, outer2, bars.outer_full, at * 64,
-                            blk0, kvh);
+                            blk0, oh);
             }
             int issued_a = 0, issued_b = 0;
             bool ok = true;
             for (int it = 0; it < tk.n && ok; ++it) {
-                const int row0 = (tk.j0 + it) * (KV ? kBQ : kBT);
+                const int row0 = (tk.j0 + it % tk.per_head) * (KV ? kBQ : kBT);
+                const int qh = KV ? bwd_query_head(a, tk, it) : tk.bh;  // head of the Q / dO tiles
                 const int sa = it % L::kSA;
                 if (it >= L::kSA) {
                     ok = mbar_wait_bounded(&bars.empty_a[sa], ((it / L::kSA) - 1) & 1u, bars.abort_flag,
@@ -240,13 +256,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                 uint8_t* st = smem + L::kRingA + sa * L::kSlotA;
                 mbar_arrive_expect_tx(&bars.full_a[sa], KV ? 2 * L::kTileIn + L::kStats : L::kTile);
                 for (int at = 0; at < D / 64; ++at) {
-                    tma_load_3d(st + at * L::kAtomIn, inner1, &bars.full_a[sa], at * 64, row0, kvh);
+                    tma_load_3d(st + at * L::kAtomIn, inner1, &bars.full_a[sa], at * 64, row0, KV ? qh : kvh);
                     if (KV)
                         tma_load_3d(st + L::kTileIn + at * L::kAtomIn, inner2, &bars.full_a[sa], at * 64, row0,
-                                    kvh);
+                                    qh);
                 }
                 if (KV) {
-                    const float* stats = a.ws + static_cast<int64_t>(tk.bh) * 2 * a.Npad + row0;
+                    const float* stats = a.ws + static_cast<int64_t>(qh) * 2 * a.Npad + row0;
                     bulk_load(st + 2 * L::kTileIn, stats, kBQ * 4, &bars.full_a[sa]);
                     bulk_load(st + 2 * L::kTileIn + kBQ * 4, stats + a.Npad, kBQ * 4, &bars.full_a[sa]);
                 }
@@ -448,7 +464,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             // of S^T and dP^T in buffer it & 1; P^T and dS^T go to the first
             // 16 and the next 16 of those S^T columns.
             for (int it = 0; it < tk.n && ok; ++it) {
-                const int jq = tk.j0 + it;  // 64-query tile index
+                const int jq = tk.j0 + it % tk.per_head;  // 64-query tile index within its head
                 const int sa = it % L::kSA;
                 ok = warp_wait(&bars.s_full[it & 1], (it >> 1) & 1u, bars.abort_flag, a.timeout_ns);
                 if (ok)  // the slot's statistics: this phase is complete and not yet refilled
@@ -643,16 +659,17 @@ cudaError_t bwd_launch_all(const BwdArgs& a, const void* o, const void* dout, co
         o, dout, lse, a.ws, a.N, a.Npad, rows_padded);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(a.num_tiles) * a.BH);
+    const unsigned grid_kv = static_cast<unsigned>(static_cast<int64_t>(a.num_tiles) * a.BHkv);
+    const unsigned grid_q = static_cast<unsigned>(static_cast<int64_t>(a.num_tiles) * a.BH);
     static bool kv_done[kMaxDevices] = {};
     static bool q_done[kMaxDevices] = {};
     auto* kkv = attn_bwd_kernel<D, BF16, true, CAUSAL>;
     if ((e = opt_in_smem(kkv, BwdLayout<D, true>::kBytes, kv_done)) != cudaSuccess) return e;
-    kkv<<<grid, kBwdThreads, BwdLayout<D, true>::kBytes, stream>>>(a);
+    kkv<<<grid_kv, kBwdThreads, BwdLayout<D, true>::kBytes, stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     auto* kq = attn_bwd_kernel<D, BF16, false, CAUSAL>;
     if ((e = opt_in_smem(kq, BwdLayout<D, false>::kBytes, q_done)) != cudaSuccess) return e;
-    kq<<<grid, kBwdThreads, BwdLayout<D, false>::kBytes, stream>>>(a);
+    kq<<<grid_q, kBwdThreads, BwdLayout<D, false>::kBytes, stream>>>(a);
     return cudaGetLastError();
 }
 

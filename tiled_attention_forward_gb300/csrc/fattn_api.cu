@@ -399,26 +399,35 @@ int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const 
               const float* lse, void* dq, void* dk, void* dv, void* workspace,
               int64_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t D, float scale,
               int causal, int dtype, fattn_stream_t stream_h) {
+    return fattn_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, H, N, D,
+                         scale, causal, dtype, stream_h);
+}
+
+int fattn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                  const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                  int64_t workspace_bytes, int64_t B, int64_t H, int64_t Hkv, int64_t N, int64_t D,
+                  float scale, int causal, int dtype, fattn_stream_t stream_h) {
     bool empty = false;
     // q, k, v and dq share the forward's rules (dq plays O's part).
-    int st = validate(q, k, v, dq, nullptr, B, H, H, N, D, scale, dtype, &empty);
+    int st = validate(q, k, v, dq, nullptr, B, H, Hkv, N, D, scale, dtype, &empty);
     if (st != FATTN_OK || empty) return st;
     if (dtype == FATTN_F32) return FATTN_ERR_UNSUPPORTED;
     if (!o || !dout || !lse || !dk || !dv || !workspace) return FATTN_ERR_INVALID_ARG;
     if (!aligned16(o) || !aligned16(dout) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u))
         return FATTN_ERR_MISALIGNED;
-    const int64_t BH = B * H;
+    const int64_t BH = B * H, BHkv = B * Hkv;
     const int64_t need = fattn_bwd_workspace_bytes(B, H, N);
     if (need <= 0) return FATTN_ERR_UNSUPPORTED;
     if (bwd_padded_rows(N) / 128 * BH > 0x7fffffffll) return FATTN_ERR_UNSUPPORTED;
     if (workspace_bytes < need) return FATTN_ERR_INVALID_ARG;
     const size_t bytes = static_cast<size_t>(BH * N * D) * 2u;
+    const size_t kvbytes = static_cast<size_t>(BHkv * N * D) * 2u;
     const size_t lb = static_cast<size_t>(BH * N) * sizeof(float);
     const void* ins[6] = {q, k, v, o, dout, lse};
-    const size_t in_sz[6] = {bytes, bytes, bytes, bytes, bytes, lb};
+    const size_t in_sz[6] = {bytes, kvbytes, kvbytes, bytes, bytes, lb};
     void* outs[4] = {dq, dk, dv, workspace};
-    const size_t out_sz[4] = {bytes, bytes, bytes, static_cast<size_t>(need)};
+    const size_t out_sz[4] = {bytes, kvbytes, kvbytes, static_cast<size_t>(need)};
     for (int i = 0; i < 4; ++i) {
         for (int j = 0; j < 6; ++j)
             if (overlaps(outs[i], out_sz[i], ins[j], in_sz[j])) return FATTN_ERR_INVALID_ARG;
@@ -433,7 +442,7 @@ int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const 
     std::memset(&a, 0, sizeof(a));
     TcArgs t;
     std::memset(&t, 0, sizeof(t));
-    if (tc_encode_maps(t, q, k, v, BH, BH, N, D, bf16) != cudaSuccess) return FATTN_ERR_CUDA;
+    if (tc_encode_maps(t, q, k, v, BH, BHkv, N, D, bf16) != cudaSuccess) return FATTN_ERR_CUDA;
     a.tmap_q = t.tmap_q;
     a.tmap_k = t.tmap_k;
     a.tmap_v = t.tmap_v;
@@ -449,6 +458,9 @@ int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const 
     a.N = static_cast<int>(N);
     a.Npad = static_cast<int>(bwd_padded_rows(N));
     a.BH = static_cast<int>(BH);
+    a.H = static_cast<int>(H);
+    a.Hkv = static_cast<int>(Hkv);
+    a.BHkv = static_cast<int>(BHkv);
     a.num_tiles = a.Npad / 128;
     a.sl2 = scale * kLog2e;
     a.scale = scale;

@@ -91,7 +91,10 @@ struct BwdArgs {
     void* dv;
     int N;
     int Npad;             // N rounded up to 128
-    int BH;
+    int BH;               // B * H query heads
+    int H;                // query heads per batch
+    int Hkv;              // key/value heads per batch (H % Hkv == 0)
+    int BHkv;             // B * Hkv
     int num_tiles;        // Npad / 128
     float sl2;            // scale * log2(e)
     float scale;
