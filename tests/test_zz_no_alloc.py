@@ -113,6 +113,9 @@ def test_static_allocates_nothing_and_reuses_the_array_in_order():
     fattn.fwd_unfused_static(*dev[0], causal=True, scale=scale, out=outs[0], lse=lses[0])
     torch.cuda.synchronize()
     assert fattn.get_device_status() == 0  # every module the status call touches is loaded now
+    import gc
+    gc.collect()  # garbage of earlier tests must not be released inside the measured window
+    torch.cuda.synchronize()
     free0, _ = torch.cuda.mem_get_info()
     alloc0 = torch.cuda.memory_allocated()
     for d, o, l in zip(dev, outs, lses):
@@ -120,7 +123,7 @@ def test_static_allocates_nothing_and_reuses_the_array_in_order():
     torch.cuda.synchronize()
     assert fattn.get_device_status() == 0
     assert torch.cuda.mem_get_info()[0] == free0
-    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.cuda.memory_allocated() <= alloc0  # nothing allocated through torch either
     for x, o, l in zip(xs, outs, lses):
         o_ref, lse_ref = oracle.attention(*(to_f64(t) for t in x), scale, True)
         compare(to_f64(o), o_ref, to_f64(l), lse_ref, torch.bfloat16, "static in order")
