@@ -113,15 +113,21 @@ FATTN_API int fattn_fwd_gqa(const void* q, const void* k, const void* v, void* o
 
 /*
  * fattn_fwd_host -- the same forward for callers holding the tensors in host
- * memory: enqueues on `stream` the host->device copies of q, k, v into the
- * caller's device buffers q_dev, k_dev, v_dev, the forward kernel writing
- * o_dev / lse_dev, and the device->host copies of O (and LSE when both
- * lse_host and lse_dev are non-NULL) into o_host / lse_host.  One
- * cudaMemcpyAsync per tensor.  Host buffers should be page-locked for the
- * copies to be asynchronous; the call returns once everything is enqueued, so
- * the caller synchronises `stream` before reading o_host.  Argument rules are
- * those of fattn_fwd, applied to the device buffers; host pointers must be
- * non-NULL.
+ * memory: the host->device copies of q, k, v into the caller's device buffers
+ * q_dev, k_dev, v_dev, the forward kernel writing o_dev / lse_dev, and the
+ * device->host copies of O (and LSE when both lse_host and lse_dev are
+ * non-NULL) into o_host / lse_host.  For bf16 / fp16 the heads are split into
+ * up to four groups so that the copies of one group overlap the kernel of
+ * the previous one (fp32: one group).  Host->device copies run on an
+ * internal copy-in stream, the kernels on `stream`, device->host copies on an
+ * internal copy-out stream, chained with events; the work starts after
+ * everything already enqueued on `stream`, and everything enqueued on
+ * `stream` afterwards waits for all of it, so the caller synchronises
+ * `stream` before reading o_host.  The first call on a device creates the two
+ * streams and ten events (kept for the process lifetime; no memory is
+ * allocated); enqueueing is serialised by a host mutex.  Host buffers should
+ * be page-locked for the copies to overlap.  Argument rules are those of
+ * fattn_fwd, applied to the device buffers; host pointers must be non-NULL.
  */
 FATTN_API int fattn_fwd_host(const void* q_host, const void* k_host, const void* v_host,
                    void* o_host, float* lse_host,

@@ -139,6 +139,39 @@ def test_host_buffer_entry_point_matches_device_entry_point():
         assert torch.equal(o_host, o_ref.cpu()) and torch.equal(lse_host, l_ref.cpu())
 
 
+@pytest.mark.parametrize("BH", [(1, 1), (1, 3), (2, 5), (4, 16)])
+def test_host_entry_point_chunked_and_ordered(BH):
+    """The host entry splits the heads into up to four groups on internal
+    copy streams: results match the device entry bit for bit for head counts
+    below, at and above the group count, with and without LSE, on a
+    non-default stream, and later work on that stream sees O and LSE."""
+    B, H = BH
+    N, D = 333, 64
+    q, k, v = make_qkv(B, H, N, D, "fp16", 77)
+    pin = [t.pin_memory() for t in (q, k, v)]
+    dev = [torch.empty_like(t, device="cuda") for t in (q, k, v)]
+    o_dev = torch.empty_like(dev[0])
+    lse_dev = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    o_ref, l_ref = fattn.fwd(q.cuda(), k.cuda(), v.cuda(), causal=False)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    for with_lse in (True, False):
+        o_host = torch.full_like(q, float("nan")).pin_memory()
+        lse_host = torch.full((B, H, N), float("nan"), dtype=torch.float32).pin_memory()
+        o_dev.fill_(float("nan"))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            fattn.fwd_host(*pin, *dev, o_dev, o_host, lse_dev if with_lse else None,
+                           lse_host if with_lse else None, causal=False, stream=s)
+            o_copy = o_dev.clone()  # enqueued after the call on the same stream
+        s.synchronize()
+        assert fattn.get_device_status() == 0
+        assert torch.equal(o_host, o_ref.cpu())
+        assert torch.equal(o_copy, o_ref)
+        if with_lse:
+            assert torch.equal(lse_host, l_ref.cpu())
+
+
 def test_empty_inputs():
     q = torch.empty(1, 2, 0, 64, dtype=torch.bfloat16, device="cuda")
     o, lse = fattn.fwd(q, q, q)

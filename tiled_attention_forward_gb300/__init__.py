@@ -171,9 +171,11 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, return_lse=True, 
 
 def fwd_host(q_host, k_host, v_host, q_dev, k_dev, v_dev, o_dev, o_host, lse_dev=None,
              lse_host=None, causal=False, scale=None, stream=None):
-    """End-to-end forward from host tensors: host->device copies, the kernel and
-    the device->host copy of O (and LSE) are all enqueued by the library on
-    ``stream``.  Host tensors should be pinned; the caller synchronises."""
+    """End-to-end forward from host tensors: host->device copies, the kernels and
+    the device->host copies of O (and LSE) are enqueued by the library, in up
+    to four groups of heads so that copies overlap the kernels (two internal
+    copy streams, joined to ``stream`` with events).  Host tensors should be
+    pinned; the caller synchronises ``stream``."""
     _check_qkv(q_host, k_host, v_host)
     B, H, N, D = q_host.shape
     if scale is None:

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <cudaTypedefs.h>
 
 #include "fattn.h"
@@ -116,6 +117,47 @@ cudaError_t encode_rows_map(CUtensorMap* map, const void* ptr, int64_t heads, in
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Per-device helpers of fattn_fwd_host: a copy-in stream, a copy-out stream
+// and the events that chain them to the caller's stream, created on the first
+// call on the device and kept for the process lifetime.
+constexpr int kHostChunks = 4;
+
+struct HostPipe {
+    cudaStream_t in = nullptr;
+    cudaStream_t out = nullptr;
+    cudaEvent_t fork = nullptr;
+    cudaEvent_t join = nullptr;
+    cudaEvent_t in_done[kHostChunks] = {};
+    cudaEvent_t k_done[kHostChunks] = {};
+    bool ready = false;
+};
+
+HostPipe g_host_pipes[kMaxDevices];
+std::mutex g_host_mu;  // also serialises the enqueue sequence of fattn_fwd_host
+
+cudaError_t host_pipe(HostPipe** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    HostPipe& p = g_host_pipes[dev];
+    if (!p.ready) {
+        const unsigned ev = cudaEventDisableTiming;
+        if ((e = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&p.fork, ev)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&p.join, ev)) != cudaSuccess)
+            return e;
+        for (int c = 0; c < kHostChunks; ++c)
+            if ((e = cudaEventCreateWithFlags(&p.in_done[c], ev)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&p.k_done[c], ev)) != cudaSuccess)
+                return e;
+        p.ready = true;
+    }
+    *out = &p;
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -294,19 +336,50 @@ int fattn_fwd_host(const void* q_host, const void* k_host, const void* v_host, v
     int st = validate(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, H, N, D, scale, dtype, &empty);
     if (st != FATTN_OK || empty) return st;
     if (!q_host || !k_host || !v_host || !o_host) return FATTN_ERR_INVALID_ARG;
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
-    const size_t bytes = static_cast<size_t>(B * H * N * D) * elem_bytes(dtype);
-    if (cudaMemcpyAsync(q_dev, q_host, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-        cudaMemcpyAsync(k_dev, k_host, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-        cudaMemcpyAsync(v_dev, v_host, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-        return FATTN_ERR_CUDA;
-    st = fattn_fwd(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, N, D, scale, causal, dtype, stream_h);
+    int sms = 0;
+    st = current_sm_count(&sms);
     if (st != FATTN_OK) return st;
-    if (cudaMemcpyAsync(o_host, o_dev, bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    HostPipe* p = nullptr;
+    if (host_pipe(&p) != cudaSuccess) return FATTN_ERR_CUDA;
+    // Heads in up to kHostChunks groups: the copies of group c+1 run on the
+    // copy-in stream while the kernel of group c runs on `stream`, and O of
+    // group c returns on the copy-out stream meanwhile.  The fp32 kernel runs
+    // far longer than the copies and loses more to the partial last wave of
+    // each group than the overlap gains, so it runs as one group.
+    const int64_t BH = B * H;
+    const int chunks = dtype == FATTN_F32 ? 1 : static_cast<int>(std::min<int64_t>(kHostChunks, BH));
+    const size_t row = static_cast<size_t>(N * D) * elem_bytes(dtype);  // one head of Q, K, V or O
+    const bool with_lse = lse_host && lse_dev;
+    auto bptr = [](const void* base, size_t off) {
+        return static_cast<void*>(static_cast<uint8_t*>(const_cast<void*>(base)) + off);
+    };
+    if (cudaEventRecord(p->fork, stream) != cudaSuccess || cudaStreamWaitEvent(p->in, p->fork, 0) != cudaSuccess)
         return FATTN_ERR_CUDA;
-    if (lse_host && lse_dev &&
-        cudaMemcpyAsync(lse_host, lse_dev, static_cast<size_t>(B * H * N) * sizeof(float),
-                        cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    for (int c = 0; c < chunks; ++c) {
+        const int64_t h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks;
+        const size_t off = static_cast<size_t>(h0) * row, len = static_cast<size_t>(h1 - h0) * row;
+        if (cudaMemcpyAsync(bptr(q_dev, off), bptr(q_host, off), len, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
+            cudaMemcpyAsync(bptr(k_dev, off), bptr(k_host, off), len, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
+            cudaMemcpyAsync(bptr(v_dev, off), bptr(v_host, off), len, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
+            cudaEventRecord(p->in_done[c], p->in) != cudaSuccess ||
+            cudaStreamWaitEvent(stream, p->in_done[c], 0) != cudaSuccess)
+            return FATTN_ERR_CUDA;
+        float* lse_c = lse_dev ? lse_dev + h0 * N : nullptr;
+        st = fattn_fwd(bptr(q_dev, off), bptr(k_dev, off), bptr(v_dev, off), bptr(o_dev, off), lse_c, 1,
+                       h1 - h0, N, D, scale, causal, dtype, stream_h);
+        if (st != FATTN_OK) return st;
+        if (cudaEventRecord(p->k_done[c], stream) != cudaSuccess ||
+            cudaStreamWaitEvent(p->out, p->k_done[c], 0) != cudaSuccess ||
+            cudaMemcpyAsync(bptr(o_host, off), bptr(o_dev, off), len, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
+            return FATTN_ERR_CUDA;
+        if (with_lse &&
+            cudaMemcpyAsync(lse_host + h0 * N, lse_dev + h0 * N, static_cast<size_t>((h1 - h0) * N) * sizeof(float),
+                            cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
+            return FATTN_ERR_CUDA;
+    }
+    if (cudaEventRecord(p->join, p->out) != cudaSuccess || cudaStreamWaitEvent(stream, p->join, 0) != cudaSuccess)
         return FATTN_ERR_CUDA;
     return FATTN_OK;
 }
