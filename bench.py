@@ -176,7 +176,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -204,7 +204,7 @@ class ClockSampler:
         if not inside:  # region shorter than the sampling period: nearest samples
             near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))[:3]
             inside = [s for (_, s) in near]
-            window = "nearest samples to a timed region shorter than the 100 ms sampling period"
+            window = "nearest samples to a timed region shorter than the 25 ms sampling period"
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
                     "note": "nvidia-smi unavailable"}
@@ -627,7 +627,7 @@ def run_reference(args, w, ws, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference", "unfused"])
