@@ -193,6 +193,27 @@ FATTN_API int fattn_bwd_gqa(const void* q, const void* k, const void* v, const v
                   fattn_stream_t stream);
 
 /*
+ * fattn_bwd_host -- the backward for callers holding the tensors in host
+ * memory (multi-head, bf16 / fp16): host->device copies of q, k, v, o, dout
+ * and lse into the caller's device buffers, the backward writing dq_dev,
+ * dk_dev, dv_dev (with the caller's workspace, sized by
+ * fattn_bwd_workspace_bytes), and device->host copies of the three
+ * gradients, in up to four groups of heads whose copies overlap the previous
+ * group's kernels, on the internal copy streams of fattn_fwd_host (same
+ * ordering against `stream`, same first-call and mutex rules).  Argument
+ * rules are those of fattn_bwd, applied to the device buffers; host pointers
+ * must be non-NULL.
+ */
+FATTN_API int fattn_bwd_host(const void* q_host, const void* k_host, const void* v_host,
+                   const void* o_host, const void* dout_host, const float* lse_host,
+                   void* dq_host, void* dk_host, void* dv_host,
+                   void* q_dev, void* k_dev, void* v_dev, void* o_dev, void* dout_dev,
+                   float* lse_dev, void* dq_dev, void* dk_dev, void* dv_dev,
+                   void* workspace, int64_t workspace_bytes,
+                   int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal,
+                   int dtype, fattn_stream_t stream);
+
+/*
  * fattn_unfused_workspace_bytes -- bytes of device workspace fattn_fwd_unfused
  * needs for B*H heads of length N: S fp32 [B*H][N][Np] followed by P 16-bit
  * [B*H][N][Np], Np = N rounded up to a multiple of 8, i.e. 6 * B*H*N*Np.

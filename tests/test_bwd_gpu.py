@@ -197,3 +197,28 @@ def test_bwd_gqa_dq_equals_mha_on_repeated_heads():
     torch.cuda.synchronize()
     assert fattn.get_device_status() == 0
     assert torch.equal(dq1, dq2)
+
+
+@pytest.mark.parametrize("BH", [(1, 3), (2, 4)])
+def test_bwd_host_entry_matches_device_entry(BH):
+    """The host-buffer backward (groups of heads with overlapped copies)
+    gives the device entry's gradients bit for bit, on a non-default stream."""
+    B, H = BH
+    N, D = 333, 128
+    q, k, v, do = make(B, H, N, D, torch.bfloat16, 123)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fattn.fwd(qd, kd, vd, causal=True)
+    ref = fattn.bwd(qd, kd, vd, o, lse, dod, causal=True)
+    torch.cuda.synchronize()
+    hosts = [t.cpu().pin_memory() for t in (q, k, v, o, do, lse)]
+    devs = [torch.empty_like(t, device="cuda") for t in hosts]
+    grads_h = [torch.full_like(q, float("nan")).pin_memory() for _ in range(3)]
+    grads_d = [torch.empty_like(qd) for _ in range(3)]
+    ws = torch.empty(fattn.bwd_workspace_bytes(B, H, N), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fattn.bwd_host(hosts, devs, grads_h, grads_d, ws, causal=True, stream=s)
+    s.synchronize()
+    assert fattn.get_device_status() == 0
+    for got, want in zip(grads_h, ref):
+        assert torch.equal(got, want.cpu())

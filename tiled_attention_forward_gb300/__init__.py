@@ -18,7 +18,7 @@ import os
 
 import torch
 
-__all__ = ["fwd", "fwd_host", "bwd", "bwd_workspace_bytes", "fwd_unfused", "fwd_unfused_static", "unfused_workspace_bytes",
+__all__ = ["fwd", "fwd_host", "bwd", "bwd_host", "bwd_workspace_bytes", "fwd_unfused", "fwd_unfused_static", "unfused_workspace_bytes",
            "UNFUSED_STATIC_BYTES", "plan", "get_device_status", "selftest_wait_timeout",
            "status_string", "library_path", "load", "FattnError", "FattnLibraryMissing",
            "DTYPE_CODES", "STATUS"]
@@ -73,6 +73,7 @@ def load():
                               ci, ci, vp]
     lib.fattn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                   i64, f32, ci, ci, vp]
+    lib.fattn_bwd_host.argtypes = [vp] * 19 + [i64, i64, i64, i64, i64, f32, ci, ci, vp]
     lib.fattn_bwd_workspace_bytes.argtypes = [i64, i64, i64]
     lib.fattn_bwd_workspace_bytes.restype = i64
     lib.fattn_fwd_unfused_static.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, ci, ci, vp]
@@ -84,7 +85,7 @@ def load():
     lib.fattn_status_string.argtypes = [ci]
     lib.fattn_status_string.restype = ctypes.c_char_p
     lib.fattn_version.argtypes = []
-    for f in ("fattn_fwd", "fattn_fwd_gqa", "fattn_fwd_host", "fattn_fwd_unfused", "fattn_bwd", "fattn_bwd_gqa",
+    for f in ("fattn_fwd", "fattn_fwd_gqa", "fattn_fwd_host", "fattn_fwd_unfused", "fattn_bwd", "fattn_bwd_gqa", "fattn_bwd_host",
               "fattn_fwd_unfused_static", "fattn_plan", "fattn_get_device_status",
               "fattn_selftest_wait_timeout", "fattn_version"):
         getattr(lib, f).restype = ci
@@ -235,6 +236,28 @@ def bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None, dv=No
                                _stream_handle(stream))
     _check(rc, "fattn_bwd_gqa")
     return dq, dk, dv
+
+
+def bwd_host(hosts, devs, grads_host, grads_dev, workspace, causal=False, scale=None, stream=None):
+    """End-to-end backward from host tensors (multi-head, bfloat16 / float16).
+
+    hosts = (q, k, v, o, dout, lse) pinned host tensors; devs = the matching
+    device buffers; grads_host / grads_dev = (dq, dk, dv) host / device
+    buffers; workspace as for ``bwd``.  Copies in, the backward and copies
+    out are enqueued by the library in groups of heads that overlap; the
+    caller synchronises ``stream``."""
+    q = hosts[0]
+    B, H, N, D = q.shape
+    if scale is None:
+        scale = _default_scale(D)
+    ptrs = [t.data_ptr() for t in hosts] + [t.data_ptr() for t in grads_host] + \
+        [t.data_ptr() for t in devs] + [t.data_ptr() for t in grads_dev] + [workspace.data_ptr()]
+    lib = load()
+    with torch.cuda.device(devs[0].device):
+        rc = lib.fattn_bwd_host(*ptrs, workspace.numel() * workspace.element_size(), B, H, N, D,
+                                float(scale), int(bool(causal)), DTYPE_CODES[q.dtype],
+                                _stream_handle(stream))
+    _check(rc, "fattn_bwd_host")
 
 
 def unfused_workspace_bytes(B, H, N):

@@ -543,6 +543,79 @@ int fattn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, co
     return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
+int fattn_bwd_host(const void* q_host, const void* k_host, const void* v_host, const void* o_host,
+                   const void* dout_host, const float* lse_host, void* dq_host, void* dk_host,
+                   void* dv_host, void* q_dev, void* k_dev, void* v_dev, void* o_dev, void* dout_dev,
+                   float* lse_dev, void* dq_dev, void* dk_dev, void* dv_dev, void* workspace,
+                   int64_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t D, float scale,
+                   int causal, int dtype, fattn_stream_t stream_h) {
+    bool empty = false;
+    int st = validate(q_dev, k_dev, v_dev, dq_dev, nullptr, B, H, H, N, D, scale, dtype, &empty);
+    if (st != FATTN_OK || empty) return st;
+    if (!q_host || !k_host || !v_host || !o_host || !dout_host || !lse_host || !dq_host || !dk_host ||
+        !dv_host)
+        return FATTN_ERR_INVALID_ARG;
+    if (dtype == FATTN_F32) return FATTN_ERR_UNSUPPORTED;
+    if (!o_dev || !dout_dev || !lse_dev || !dk_dev || !dv_dev || !workspace) return FATTN_ERR_INVALID_ARG;
+    const int64_t need = fattn_bwd_workspace_bytes(B, H, N);
+    if (need <= 0) return FATTN_ERR_UNSUPPORTED;
+    if (workspace_bytes < need) return FATTN_ERR_INVALID_ARG;
+    int sms = 0;
+    st = current_sm_count(&sms);
+    if (st != FATTN_OK) return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    HostPipe* p = nullptr;
+    if (host_pipe(&p) != cudaSuccess) return FATTN_ERR_CUDA;
+    // As fattn_fwd_host: groups of heads whose copies overlap the previous
+    // group's three kernels.  A group's statistics use its own slice of the
+    // workspace ([heads][2][Npad] floats).
+    const int64_t BH = B * H;
+    const int chunks = static_cast<int>(std::min<int64_t>(kHostChunks, BH));
+    const size_t row = static_cast<size_t>(N * D) * 2u;  // one head of a 16-bit tensor
+    const int64_t ws_head = need / BH;                   // bytes of workspace per head
+    auto bptr = [](const void* base, size_t off) {
+        return static_cast<void*>(static_cast<uint8_t*>(const_cast<void*>(base)) + off);
+    };
+    if (cudaEventRecord(p->fork, stream) != cudaSuccess || cudaStreamWaitEvent(p->in, p->fork, 0) != cudaSuccess)
+        return FATTN_ERR_CUDA;
+    for (int c = 0; c < chunks; ++c) {
+        const int64_t h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks;
+        const size_t off = static_cast<size_t>(h0) * row, len = static_cast<size_t>(h1 - h0) * row;
+        const size_t loff = static_cast<size_t>(h0 * N) * sizeof(float);
+        const size_t llen = static_cast<size_t>((h1 - h0) * N) * sizeof(float);
+        const void* hin[5] = {q_host, k_host, v_host, o_host, dout_host};
+        void* din[5] = {q_dev, k_dev, v_dev, o_dev, dout_dev};
+        for (int t = 0; t < 5; ++t)
+            if (cudaMemcpyAsync(bptr(din[t], off), bptr(hin[t], off), len, cudaMemcpyHostToDevice, p->in) !=
+                cudaSuccess)
+                return FATTN_ERR_CUDA;
+        if (cudaMemcpyAsync(bptr(lse_dev, loff), bptr(lse_host, loff), llen, cudaMemcpyHostToDevice, p->in) !=
+                cudaSuccess ||
+            cudaEventRecord(p->in_done[c], p->in) != cudaSuccess ||
+            cudaStreamWaitEvent(stream, p->in_done[c], 0) != cudaSuccess)
+            return FATTN_ERR_CUDA;
+        st = fattn_bwd(bptr(q_dev, off), bptr(k_dev, off), bptr(v_dev, off), bptr(o_dev, off),
+                       bptr(dout_dev, off), reinterpret_cast<const float*>(bptr(lse_dev, loff)),
+                       bptr(dq_dev, off), bptr(dk_dev, off), bptr(dv_dev, off),
+                       bptr(workspace, static_cast<size_t>(h0 * ws_head)), (h1 - h0) * ws_head, 1, h1 - h0,
+                       N, D, scale, causal, dtype, stream_h);
+        if (st != FATTN_OK) return st;
+        if (cudaEventRecord(p->k_done[c], stream) != cudaSuccess ||
+            cudaStreamWaitEvent(p->out, p->k_done[c], 0) != cudaSuccess)
+            return FATTN_ERR_CUDA;
+        void* hout[3] = {dq_host, dk_host, dv_host};
+        void* dout3[3] = {dq_dev, dk_dev, dv_dev};
+        for (int t = 0; t < 3; ++t)
+            if (cudaMemcpyAsync(bptr(hout[t], off), bptr(dout3[t], off), len, cudaMemcpyDeviceToHost, p->out) !=
+                cudaSuccess)
+                return FATTN_ERR_CUDA;
+    }
+    if (cudaEventRecord(p->join, p->out) != cudaSuccess || cudaStreamWaitEvent(stream, p->join, 0) != cudaSuccess)
+        return FATTN_ERR_CUDA;
+    return FATTN_OK;
+}
+
 int fattn_get_device_status(fattn_stream_t stream_h) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FATTN_ERR_CUDA;
