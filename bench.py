@@ -1,7 +1,7 @@
 """Benchmark of the attention forward on GB300 (one JSON line on stdout).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference|unfused] [--pass fwd|bwd]
+                    [--impl ours|reference|unfused|rowwise] [--pass fwd|bwd]
 
 A step is one attention forward (the whole hot path: one kernel launch) over
 the named workload's synthetic seeded inputs, already resident in HBM.
@@ -33,6 +33,9 @@ backward on whole heads of the workload.
 (fattn_fwd_unfused: S and P written to HBM, three kernels per step) on the
 same workload, inputs and timing rules, for the HBM-traffic comparison; its
 roofline is the HBM bound of the whole three-kernel step.
+
+`--impl rowwise` (fp32 workloads) times fattn_fwd_f32_rowwise, the fp32
+kernel with one query row per thread, under the same rules (no e2e leg).
 """
 import argparse
 import json
@@ -59,33 +62,39 @@ BWD_FLOP_FACTOR = 2.5
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the forward kernel on each workload, from an ncu capture (summaries under
-# profiles/), tagged with the hash of the forward kernels' device sources it
-# was taken on.  Reported only while those sources still hash the same; null
-# once a kernel has changed.
-KERNEL_SOURCES = ["fwd_tc.cu", "fwd_ffma.cu", "sm103_ptx.cuh"]
+# profiles/), tagged with the hash of that kernel's device sources when it
+# was taken.  Reported only while those sources still hash the same; null
+# once the kernel has changed.
+KERNEL_SOURCES = {"tc": ["fwd_tc.cu", "sm103_ptx.cuh"], "ffma": ["fwd_ffma.cu"]}
 NCU_TRAFFIC = {
-    "bf16_B4_H16_N4096_D128": (201617152 + 35978240, "7468ab8e5ed26c85"),
-    "bf16_B2_H32_N8192_D128_causal_qstd4": (2664641536 + 126893056, "7468ab8e5ed26c85"),
-    "fp16_B1_H16_N16000_D64_causal": (124670976 + 13032448, "7468ab8e5ed26c85"),
-    "fp32_B4_H8_N8192_D64_causal": (201591552 + 51286272, "7468ab8e5ed26c85"),
+    "bf16_B4_H16_N4096_D128": (201401344 + 37292544, "e063c77b0f7d82be"),
+    "bf16_B2_H32_N8192_D128_causal_qstd4": (2542723072 + 127336704, "e063c77b0f7d82be"),
+    "fp16_B1_H16_N16000_D64_causal": (127892736 + 14467072, "e063c77b0f7d82be"),
+    "fp32_B4_H8_N8192_D64_causal": (201690624 + 51116544, "224b5f7dc90ca5e2"),
 }
 
 
-def kernel_source_hash():
+def kernel_family(w):
+    return "ffma" if w.dtype == "fp32" else "tc"
+
+
+def kernel_source_hash(family):
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tiled_attention_forward_gb300", "csrc")
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[family]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload):
-    entry = NCU_TRAFFIC.get(workload)
-    if entry is None or entry[1] != kernel_source_hash():
+def ncu_traffic(w):
+    entry = NCU_TRAFFIC.get(w.name)
+    if entry is None or entry[1] != kernel_source_hash(kernel_family(w)):
         return None
     return entry[0]
+
+
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
@@ -270,6 +279,9 @@ def run_ours(args, w, ws, rank, local):
     stream = torch.cuda.current_stream(dev)
 
     unfused = args.impl == "unfused"
+    rowwise = args.impl == "rowwise"
+    if rowwise and w.dtype != "fp32":
+        raise SystemExit("--impl rowwise covers fp32 workloads only")
     if unfused:
         if w.dtype == "fp32":
             raise SystemExit("--impl unfused covers bf16 / fp16 workloads only")
@@ -279,6 +291,9 @@ def run_ours(args, w, ws, rank, local):
         if unfused:
             fattn.fwd_unfused(qd, kd, vd, causal=w.causal, scale=w.scale, out=o, lse=lse,
                               workspace=wsp, stream=stream)
+        elif rowwise:
+            fattn.fwd_f32_rowwise(qd, kd, vd, causal=w.causal, scale=w.scale, out=o, lse=lse,
+                                  stream=stream)
         else:
             fattn.fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream)
 
@@ -320,7 +335,7 @@ def run_ours(args, w, ws, rank, local):
 
     # end to end through the host-buffer entry point
     e2e_ms, h2d, d2h = float("nan"), 0, 0
-    if not args.no_e2e and not unfused:
+    if not args.no_e2e and not unfused and not rowwise:
         e2e_ms, h2d, d2h = run_e2e(fattn, w, q, k, v, qd, kd, vd, o, lse, stream, dev, args.steps, barrier)
     ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], device=dev)
     clocks = sampler.summary(t0, t1)
@@ -347,19 +362,19 @@ def run_ours(args, w, ws, rank, local):
         sm_mhz = peaks.get("sm_max_mhz", 2070.0)
         peak = torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT,
-                "frac": achieved / peak, "traffic": ncu_traffic(w.name),
+                "frac": achieved / peak, "traffic": ncu_traffic(w) if not rowwise else None,
                 "peak_source": "FP32 FFMA: SMs x 128 lanes x 2 FLOP x max SM clock (%s clock)" % peak_src}
     else:
         peak = float(peaks[peak_key])
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                "frac": achieved / peak, "traffic": ncu_traffic(w.name),
+                "frac": achieved / peak, "traffic": ncu_traffic(w) if not rowwise else None,
                 "peak_source": "%s dense bf16 (cuBLAS burst) of %s; fp16 taken at the same rate"
                                % (peak_key, peak_src),
                 "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak))}
     roof["traffic_note"] = "see profiles/ for ncu DRAM bytes" if unfused else ("DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum); "
                             "algorithmic compulsory bytes (Q+K+V read, O+LSE write): %d" % w_bytes(w))
-    if unfused:
-        line_extra = {"impl": "unfused"}
+    if unfused or rowwise:
+        line_extra = {"impl": args.impl}
     else:
         line_extra = {}
     line = {
@@ -371,11 +386,11 @@ def run_ours(args, w, ws, rank, local):
         "e2e": ({"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                  "ms_per_step": e2e_ms, "api": "fattn_fwd_host (pinned host buffers)"}
-                if not (args.no_e2e or unfused) else None),
+                if not (args.no_e2e or unfused or rowwise) else None),
         "gpu_launches": launches, "clocks": clocks,
     }
     line.update(line_extra)
-    if not args.no_cpu_baseline and not unfused:
+    if not args.no_cpu_baseline and not unfused and not rowwise:
         q64, k64, v64 = (t.to(torch.float64).numpy() for t in (q, k, v))
         fl, secs, nrows, threads = oracle_rows_rate(w, q64, k64, v64, args.cpu_seconds, 1)
         line["cpu_baseline"] = {"value": fl / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -629,7 +644,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference", "unfused"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference", "unfused", "rowwise"])
     ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall time of the CPU oracle sample (cpu_baseline)")
@@ -641,8 +656,8 @@ def main():
     ws, rank, local = dist_env()
     w = BY_NAME[args.workload]
     if args.pass_ == "bwd":
-        if args.impl == "unfused":
-            ap.error("--impl unfused is a forward comparator")
+        if args.impl in ("unfused", "rowwise"):
+            ap.error("--impl %s is a forward variant" % args.impl)
         line = run_reference_bwd(args, w, ws, rank) if args.impl == "reference" else \
             run_ours_bwd(args, w, ws, rank, local)
     elif args.impl == "reference":

@@ -24,7 +24,9 @@
  * Paths: FATTN_BF16 / FATTN_F16 run the tensor-core kernel (TMA, tcgen05 MMA
  * with TMEM accumulators, fp32 accumulation and softmax, P rounded to the
  * input dtype for the P.V product).  FATTN_F32 runs a CUDA-core FFMA kernel
- * (one query row per thread, fp32 throughout).  Supported head dims: 64, 128.
+ * (register micro-tiles of 8 query rows per thread, fp32 throughout;
+ * fattn_fwd_f32_rowwise runs the one-row-per-thread form).  Supported head
+ * dims: 64, 128.
  *
  * Ownership: the caller owns every buffer.  No entry point allocates device
  * or pinned host memory, and nothing is retained after a call returns except
@@ -110,6 +112,22 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, fl
 FATTN_API int fattn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
                   int64_t B, int64_t H, int64_t Hkv, int64_t N, int64_t D, float scale,
                   int causal, int dtype, fattn_stream_t stream);
+
+/*
+ * fattn_fwd_f32_rowwise -- the fp32 forward in the CUDA-core layout of the
+ * dandandamowang.xyz "Flash Attention (二) v2" page (§1.1, §3.2-§3.5): one
+ * query row per thread, Br = 128 threads per CTA, Bc = 32 keys per K/V tile
+ * at D = 64 (16 at D = 128), double-buffered cp.async K/V, padded shared
+ * memory, grid (ceil(N/128), B*H).  Same arguments, results (to fp32
+ * rounding), validation and error behaviour as fattn_fwd with dtype ==
+ * FATTN_F32; one kernel launch per call.  fattn_fwd's own fp32 kernel
+ * spreads each CTA's 128 rows over 256 threads as register micro-tiles and
+ * is faster on this part; this entry point keeps the page's layout
+ * available and measurable.
+ */
+FATTN_API int fattn_fwd_f32_rowwise(const float* q, const float* k, const float* v, float* o,
+                          float* lse, int64_t B, int64_t H, int64_t N, int64_t D, float scale,
+                          int causal, fattn_stream_t stream);
 
 /*
  * fattn_fwd_host -- the same forward for callers holding the tensors in host

@@ -36,7 +36,7 @@ def test_header_declares_the_boundary():
                  "fattn_get_device_status", "fattn_selftest_wait_timeout",
                  "fattn_fwd_unfused", "fattn_unfused_workspace_bytes",
                  "fattn_bwd", "fattn_bwd_gqa", "fattn_bwd_workspace_bytes",
-                 "fattn_status_string", "fattn_version"):
+                 "fattn_fwd_f32_rowwise", "fattn_status_string", "fattn_version"):
         assert name in syms
 
 
@@ -82,6 +82,21 @@ def test_argument_errors_before_any_cuda_call(lib):
     assert call_fwd(lib, N=(1 << 30) + 1) == UNSUPPORTED
     assert call_fwd(lib, B=1 << 16, H=1 << 16) == UNSUPPORTED
     assert call_fwd(lib, B=70000, H=1, dtype=0) == UNSUPPORTED
+
+
+def test_rowwise_argument_errors(lib):
+    def rw(q=FAKE, k=FAKE + (1 << 16), v=FAKE + (2 << 16), o=FAKE + (3 << 16), lse=None,
+           B=1, H=1, N=16, D=64, scale=0.125):
+        return lib.fattn_fwd_f32_rowwise(q, k, v, o, lse, B, H, N, D, scale, 0, None)
+    assert rw(q=None) == INVALID
+    assert rw(N=-1) == INVALID
+    assert rw(scale=float("nan")) == INVALID
+    assert rw(D=96) == UNSUPPORTED
+    assert rw(B=70000) == UNSUPPORTED      # grid.y limit of the fp32 launch
+    assert rw(k=FAKE + (1 << 16) + 4) == MISALIGNED
+    assert rw(o=FAKE + 32) == INVALID       # O over Q
+    assert rw(B=0) == OK
+    assert rw(N=0) == OK
 
 
 def test_gqa_argument_errors(lib):
@@ -202,29 +217,36 @@ def test_host_entry_point_argument_errors(lib):
 def test_plan_ffma_matches_page_tile_arithmetic(lib, golden_dir):
     g = json.load(open(os.path.join(golden_dir, "tile_arithmetic.json")))
     grid = g["cases"][0]
-    # fp32 path: grid = (ceil(N/Br), B*H) with Br = 128
+    # fp32 path: grid = (ceil(N/Br), B*H) with Br = 128 (the page's grid); the
+    # CTA spreads its 128 rows over 256 threads, in K/V tiles of 64 keys
     p = fattn.plan(4, 8, grid["N"], 64, causal=False, dtype=torch.float32, num_sms=152)
     assert p["path"] == 1
     assert (p["grid_x"], p["grid_y"]) == (grid["grid_x"], grid["grid_y"])
     assert p["grid_x"] * p["grid_y"] == grid["blocks"]
-    assert p["rows_per_task"] == grid["Br"] and p["threads"] == grid["Br"]
+    assert p["rows_per_task"] == grid["Br"]
+    assert p["threads"] == 256 and p["keys_per_kv_tile"] == 64
     nvec = g["cases"][1]
-    assert p["keys_per_kv_tile"] == nvec["Bc"]
     assert nvec["Bc"] * nvec["D"] * nvec["elem_bytes"] // 16 == nvec["nvec"]
     # non-causal: every Q block visits every K/V tile
-    assert p["kv_tiles"] == 64 * 32 * (8192 // 32)
+    assert p["kv_tiles"] == 64 * 32 * (8192 // p["keys_per_kv_tile"])
+
+
+def causal_tiles_per_block(N, Br, Bc):
+    # Q block qb visits ceil(min((qb+1)*Br, N)/Bc) K/V tiles
+    return [-(-min((qb + 1) * Br, N) // Bc) for qb in range(-(-N // Br))]
 
 
 def test_plan_causal_skip_counts(lib, golden_dir):
     g = json.load(open(os.path.join(golden_dir, "tile_arithmetic.json")))["cases"][2]
     N, Br, Bc = g["N"], g["Br"], g["Bc"]
-    p = fattn.plan(1, 1, N, 64, causal=True, dtype=torch.float32, num_sms=152)
-    nq = N // Br
-    # Q block qb visits ceil(min((qb+1)*Br, N)/Bc) tiles; block 5 visits 24 and skips 40
-    per_block = [min((qb + 1) * Br, N) // Bc for qb in range(nq)]
+    # the page's worked numbers: with Bc = 32, block 5 visits 24 tiles and skips 40
+    per_block = causal_tiles_per_block(N, Br, Bc)
     assert per_block[g["q_block"]] == g["tiles_visited"]
     assert N // Bc - per_block[g["q_block"]] == g["tiles_skipped"]
-    assert p["kv_tiles"] == sum(per_block)
+    p = fattn.plan(1, 1, N, 64, causal=True, dtype=torch.float32, num_sms=152)
+    assert p["kv_tiles"] == sum(causal_tiles_per_block(N, Br, p["keys_per_kv_tile"]))
+    p = fattn.plan(1, 1, 1000, 128, causal=True, dtype=torch.float32, num_sms=152)
+    assert p["kv_tiles"] == sum(causal_tiles_per_block(1000, 128, p["keys_per_kv_tile"]))
 
 
 def test_plan_tensor_core_path(lib):

@@ -65,6 +65,7 @@ def load():
     vp, i64, f32, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
     lib.fattn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, ci, ci, vp]
     lib.fattn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, ci, ci, vp]
+    lib.fattn_fwd_f32_rowwise.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, ci, vp]
     lib.fattn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                    i64, i64, i64, i64, f32, ci, ci, vp]
     lib.fattn_fwd_unfused.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, ci,
@@ -167,6 +168,31 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, return_lse=True, 
                                    lse_ptr, B, H, Hkv, N, D, float(scale), int(bool(causal)),
                                    DTYPE_CODES[q.dtype], _stream_handle(stream))
     _check(rc, "fattn_fwd" if Hkv == H else "fattn_fwd_gqa")
+    return out, (lse if return_lse else None)
+
+
+def fwd_f32_rowwise(q, k, v, causal=False, scale=None, out=None, lse=None, return_lse=True,
+                    stream=None):
+    """fp32 forward through the one-query-row-per-thread CUDA-core kernel
+    (fattn_fwd_f32_rowwise).  q, k, v: contiguous float32 CUDA tensors of one
+    shape [B, H, N, D]; otherwise as fwd."""
+    _check_qkv(q, k, v)
+    if not q.is_cuda or q.dtype != torch.float32:
+        raise ValueError("fwd_f32_rowwise needs float32 CUDA tensors")
+    B, H, N, D = q.shape
+    if scale is None:
+        scale = _default_scale(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    lse_ptr = lse.data_ptr() if (return_lse and lse is not None) else None
+    lib = load()
+    with torch.cuda.device(q.device):
+        rc = lib.fattn_fwd_f32_rowwise(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                       lse_ptr, B, H, N, D, float(scale), int(bool(causal)),
+                                       _stream_handle(stream))
+    _check(rc, "fattn_fwd_f32_rowwise")
     return out, (lse if return_lse else None)
 
 

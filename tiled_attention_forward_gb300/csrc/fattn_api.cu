@@ -248,7 +248,7 @@ int fattn_plan(int64_t B, int64_t H, int64_t N, int64_t D, int causal, int dtype
         out[0] = 1;
         out[1] = nq;
         out[2] = BH;
-        out[3] = kFfmaBr;
+        out[3] = ffma_threads(static_cast<int>(D));
         out[4] = ffma_smem_bytes(static_cast<int>(D));
         out[5] = nq * BH;
         out[6] = tiles * BH;
@@ -325,6 +325,20 @@ int fattn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* l
     a.timeout_ns = kDefaultTimeoutNs;
     const int grid = static_cast<int>(std::min<int64_t>(a.num_tasks, sms));
     cudaError_t e = tc_launch(a, static_cast<int>(D), bf16, causal != 0, grid, stream);
+    return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
+int fattn_fwd_f32_rowwise(const float* q, const float* k, const float* v, float* o, float* lse,
+                          int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal,
+                          fattn_stream_t stream_h) {
+    bool empty = false;
+    int st = validate(q, k, v, o, lse, B, H, H, N, D, scale, FATTN_F32, &empty);
+    if (st != FATTN_OK || empty) return st;
+    int sms = 0;
+    st = current_sm_count(&sms);
+    if (st != FATTN_OK) return st;
+    cudaError_t e = ffma_row_launch(q, k, v, o, lse, B * H, H, H, N, D, scale * kLog2e, causal != 0,
+                                    reinterpret_cast<cudaStream_t>(stream_h));
     return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 

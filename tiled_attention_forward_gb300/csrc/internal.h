@@ -41,12 +41,19 @@ cudaError_t tc_launch(const TcArgs& a, int D, bool bf16, bool causal, int grid,
                       cudaStream_t stream);
 
 // ---- CUDA-core path (fp32), fwd_ffma.cu --------------------------------------
-constexpr int kFfmaBr = 128;      // Q rows per CTA = threads per CTA (one row per thread)
+constexpr int kFfmaBr = 128;      // Q rows per CTA
 int ffma_bc(int D);               // keys per K/V tile
+int ffma_threads(int D);          // threads per CTA
 int ffma_smem_bytes(int D);
 cudaError_t ffma_launch(const float* q, const float* k, const float* v, float* o, float* lse,
                         int64_t BH, int64_t H, int64_t Hkv, int64_t N, int64_t D,
                         float scale_log2, bool causal, cudaStream_t stream);
+// One query row per thread (Br = 128 threads), the page's own design.
+int ffma_row_bc(int D);
+int ffma_row_smem_bytes(int D);
+cudaError_t ffma_row_launch(const float* q, const float* k, const float* v, float* o, float* lse,
+                            int64_t BH, int64_t H, int64_t Hkv, int64_t N, int64_t D,
+                            float scale_log2, bool causal, cudaStream_t stream);
 
 // ---- unfused comparator (bf16 / fp16), fwd_unfused.cu ----------------------
 struct UnfusedArgs {
