@@ -67,9 +67,9 @@ BWD_FLOP_FACTOR = 2.5
 # once the kernel has changed.
 KERNEL_SOURCES = {"tc": ["fwd_tc.cu", "sm103_ptx.cuh"], "ffma": ["fwd_ffma.cu"]}
 NCU_TRAFFIC = {
-    "bf16_B4_H16_N4096_D128": (201401344 + 37292544, "e063c77b0f7d82be"),
-    "bf16_B2_H32_N8192_D128_causal_qstd4": (2542723072 + 127336704, "e063c77b0f7d82be"),
-    "fp16_B1_H16_N16000_D64_causal": (127892736 + 14467072, "e063c77b0f7d82be"),
+    "bf16_B4_H16_N4096_D128": (201402368 + 37269760, "783ef5e313392a71"),
+    "bf16_B2_H32_N8192_D128_causal_qstd4": (2462308864 + 126794496, "783ef5e313392a71"),
+    "fp16_B1_H16_N16000_D64_causal": (127360512 + 14477568, "783ef5e313392a71"),
     "fp32_B4_H8_N8192_D64_causal": (201690624 + 51116544, "224b5f7dc90ca5e2"),
 }
 

@@ -13,7 +13,8 @@
 //
 // Warp roles (384 threads = three warpgroups):
 //   warps 0-3  softmax warpgroup 0: Q tile 0, thread t owns query row t
-//              (TMEM lane t): S row -> mask -> max -> exp2 -> P (16-bit) into
+//              (TMEM lane t): S row and its max (one reducing TMEM load,
+//              tcgen05.ld.red) -> mask -> exp2 -> P (16-bit) into
 //              TMEM, conditional O rescale, epilogue (O/l, LSE, store)
 //   warps 4-7  softmax warpgroup 1: same for Q tile 1
 //   warp 8     MMA issue (one elected lane): S_i = Q_i K_j^T (SS form),
@@ -415,33 +416,41 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
             tc_fence_after();
 
             // The whole score row: four 32-column loads in flight, one wait.
+            // The loads also reduce: cmx[c] = max of the 32 scores of chunk c
+            // (tcgen05.ld.red), the row max of every tile without masked keys.
             uint32_t sr[kTcBN / 32][32];
+            float cmx[kTcBN / 32];
 #pragma unroll
-            for (int c = 0; c < kTcBN / 32; ++c) tmem_ld32(tS + c * 32, sr[c]);
+            for (int c = 0; c < kTcBN / 32; ++c) tmem_ld32_max(tS + c * 32, sr[c], cmx[c]);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < kTcBN / 32; ++c) reg_fence(sr[c]);
+            for (int c = 0; c < kTcBN / 32; ++c) {
+                reg_fence(sr[c]);
+                reg_fence(cmx[c]);
+            }
             float s[kTcBN];
 #pragma unroll
             for (int c = 0; c < kTcBN; ++c) s[c] = __uint_as_float(sr[c / 32][c % 32]);
 
             const int kb = j * kTcBN;
             const bool need_mask = (kb + kTcBN > a.N) || (CAUSAL && kb + kTcBN - 1 > row0);
+            float mblk = fmaxf(fmaxf(cmx[0], cmx[1]), fmaxf(cmx[2], cmx[3]));
             if (need_mask) {
+                // Keys past N or past the row: masked here, and the row max
+                // taken over the visible scores only.
                 const int vis = lim - kb;
 #pragma unroll
                 for (int c = 0; c < kTcBN; ++c)
                     if (c >= vis) s[c] = -INFINITY;
+                float mx[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) mx[u] = s[u];
+#pragma unroll
+                for (int c = 8; c < kTcBN; c += 2)
+                    mx[(c / 2) % 8] = fmax3f(mx[(c / 2) % 8], s[c], s[c + 1]);
+                mblk = fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]),
+                              fmaxf(mx[6], mx[7]));
             }
-
-            // Row max: eight independent chains of three-input max.
-            float mx[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mx[u] = s[u];
-#pragma unroll
-            for (int c = 8; c < kTcBN; c += 2) mx[(c / 2) % 8] = fmax3f(mx[(c / 2) % 8], s[c], s[c + 1]);
-            const float mblk = fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]),
-                                      fmaxf(mx[6], mx[7]));
             const float m_new = fmaxf(m_run, mblk * sl2);
 
             if (j == 0) {
