@@ -66,8 +66,12 @@ struct TcLayout {
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = kTcQTiles * kQTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kKVTileBytes;
-    // q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] drain[1]
-    static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1;
+    // D = 128: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] drain[1]
+    // D = 64 (three S buffers): ... s_full[3][2] p_full[3] o_full[2] o_ready[2] drain[1]
+    static constexpr bool kRot = (D == 64);
+    static constexpr int kSFull = kRot ? 6 : 2;
+    static constexpr int kPFull = kRot ? 3 : 2;
+    static constexpr int kNumBars = 2 + 2 + 2 * kStages + kSFull + kPFull + 2 + (kRot ? 2 : 0) + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kAlloc = kBytes;  // the dynamic base is declared 1024-byte aligned
@@ -76,7 +80,7 @@ struct TcLayout {
     // The MMA warp holds two ring slots (V_j, K_{j+1}) until the end of an
     // iteration and then needs V_{j+1} and K_{j+2}: four slots at least.
     static_assert(kStages >= 4, "K/V ring depth");
-    static_assert(256 + 2 * D <= 512, "TMEM budget");
+    static_assert((kRot ? 384 : 256) + 2 * D <= 512, "TMEM budget");
 };
 
 struct Task {
@@ -90,7 +94,7 @@ struct Task {
 // concurrently running CTAs share that head's K/V in L2).  Causal, longest
 // first: Q blocks nearest the end of the sequence (most K/V tiles) are
 // scheduled first, heads inner.
-template <bool CAUSAL>
+template <bool CAUSAL, bool EQUAL = false>
 __device__ __forceinline__ Task decode_task(int t, const TcArgs& a) {
     Task k;
     int qblk;
@@ -116,6 +120,13 @@ __device__ __forceinline__ Task decode_task(int t, const TcArgs& a) {
         }
     }
     k.nbmax = max(k.nb[0], k.nb[1]);
+    if (EQUAL) {
+        // Both tiles visit nbmax blocks: under causal masking tile 0's extra
+        // block lies wholly above its diagonal (every score masked, P = 0),
+        // and a tile 1 past N computes rows that are never stored.
+        k.nb[0] = k.nbmax;
+        k.nb[1] = k.nbmax;
+    }
     return k;
 }
 
@@ -125,8 +136,9 @@ struct Bars {
     uint64_t* kv_full;
     uint64_t* kv_empty;
     uint64_t* s_full;
-    uint64_t* p_full;  // [tile]: P_tile stored (and O_tile rescaled)
+    uint64_t* p_full;  // D = 128: [tile]; D = 64: [S buffer]: P stored (and O rescaled)
     uint64_t* o_full;
+    uint64_t* o_ready;  // D = 64: [tile], one phase per completed P.V product
     uint64_t* drain;
 };
 
@@ -140,9 +152,10 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
     r.kv_full = b + 4;
     r.kv_empty = r.kv_full + L::kStages;
     r.s_full = r.kv_empty + L::kStages;
-    r.p_full = r.s_full + 2;
-    r.o_full = r.p_full + 2;
-    r.drain = r.o_full + 2;
+    r.p_full = r.s_full + L::kSFull;
+    r.o_full = r.p_full + L::kPFull;
+    r.o_ready = r.o_full + 2;
+    r.drain = r.o_ready + (L::kRot ? 2 : 0);
     return r;
 }
 
@@ -209,7 +222,7 @@ __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
     };
 
     for (int t = blockIdx.x; t < a.num_tasks && ok; t += gridDim.x) {
-        const Task tk = decode_task<CAUSAL>(t, a);
+        const Task tk = decode_task<CAUSAL, L::kRot>(t, a);
         const int kvh = kv_head_of(tk.bh, a.H, a.Hkv);
         load_q(0, tk);
         if (!ok) break;
@@ -555,6 +568,313 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
     }
 }
 
+// ---------------------------------------------------------------------------
+// D = 64: three S buffers shared by the two Q tiles
+// ---------------------------------------------------------------------------
+// At D = 64 the TMEM holds three 128-column S buffers next to the two O
+// accumulators (3 x 128 + 2 x 64 = 512 columns).  Both Q tiles of a task visit
+// the same nb blocks (decode_task<CAUSAL, true>), and product k = 2j + i of a
+// task (tile i, K/V block j; counted on from the products of earlier tasks)
+// uses buffer k mod 3.  Per block j the MMA warp issues
+//     P.V_0(j), S_1(j+1), P.V_1(j), S_0(j+2),
+// each S going into the buffer whose P was consumed by the P.V just before it
+// (tensor-core instructions of a CTA execute in issue order).  So a tile's
+// next scores are computed while its softmax warps still work on the current
+// ones, and the MMAs leave the softmax's critical path.  Ordering facts the
+// barriers rely on: S_i(j) is issued after P.V_i(j-2), so when a softmax
+// warpgroup sees S_i(j) complete, P.V_i(j-2) is complete too, and its wait
+// for P.V_i(j-1) on o_ready[i] (only to rescale O_i) is never two phases away;
+// s_full[b * 2 + i] has one waiting warpgroup (tile i), which sees every phase;
+// the MMA warp waits for P in product order on p_full[b].
+
+template <bool BF16, bool CAUSAL>
+__device__ void mma_role_rot(const TcArgs& a, uint8_t* smem, const Bars& bars, uint32_t tmem_base,
+                             volatile uint32_t* abort_flag) {
+    constexpr int D = 64;
+    using L = TcLayout<D>;
+    constexpr uint32_t kIdescQK = idesc_f16_f32(kTcBM, kTcBN, BF16 ? 1u : 0u, 0u, 0u);
+    constexpr uint32_t kIdescPV = idesc_f16_f32(kTcBM, D, BF16 ? 1u : 0u, 0u, 1u);
+    const uint32_t q_smem = smem_u32(smem + L::kQOff);
+    const uint32_t kv_smem = smem_u32(smem + L::kKVOff);
+    const uint64_t kmaj_desc = smem_desc_sw128(0u, 16u, 1024u);          // Q, K: K-major
+    const uint64_t vmn_desc = smem_desc_sw128(0u, kTcBN * 128u, 1024u);  // V: MN-major
+
+    uint32_t kv_base = 0;  // ring position of the task's K_0 (K_j at 2j, V_j at 2j + 1)
+    uint32_t sbase = 0;    // products of earlier tasks
+    uint32_t qcnt = 0;     // tasks started (q_full phases of both tiles)
+    bool ok = true;
+
+    auto wait_pos = [&](uint32_t pos) -> uint32_t {
+        const uint32_t slot = pos % L::kStages;
+        ok = warp_wait(&bars.kv_full[slot], (pos / L::kStages) & 1u, abort_flag, a.timeout_ns);
+        tc_fence_after();
+        return slot;
+    };
+    // S product into buffer b: Q tile i against the K tile in ring slot ks.
+    auto issue_s = [&](uint32_t b, int i, uint32_t ks) {
+        const uint64_t adesc = kmaj_desc + ((q_smem + i * L::kQTileBytes) >> 4);
+        const uint64_t bdesc = kmaj_desc + ((kv_smem + ks * L::kKVTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem_base + b * kTcBN, adesc + ((kk * 32) >> 4), bdesc + ((kk * 32) >> 4),
+                   kIdescQK, kk > 0 ? 1u : 0u);
+        mma_commit(&bars.s_full[b * 2 + i]);
+    };
+    // O_i (+)= P (buffer b) V (ring slot vs).
+    auto issue_pv = [&](uint32_t b, int i, uint32_t vs, bool accumulate) {
+        const uint64_t bdesc = vmn_desc + ((kv_smem + vs * L::kKVTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kTcBN / 16; ++kk)
+            mma_ts(tmem_base + 3 * kTcBN + i * D, tmem_base + b * kTcBN + kk * 8,
+                   bdesc + ((kk * 16 * 128) >> 4), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.o_ready[i]);
+    };
+    auto wait_p = [&](uint32_t k) {
+        ok = warp_wait(&bars.p_full[k % 3u], (k / 3u) & 1u, abort_flag, a.timeout_ns);
+        tc_fence_after();
+    };
+
+    for (int t = blockIdx.x; t < a.num_tasks && ok; t += gridDim.x) {
+        const Task tk = decode_task<CAUSAL, true>(t, a);
+        const int nb = tk.nbmax;
+        // Prologue: S_0(0), S_1(0), S_0(1).
+        ok = warp_wait(&bars.q_full[0], qcnt & 1u, abort_flag, a.timeout_ns);
+        if (!ok) break;
+        uint32_t ks = wait_pos(kv_base);
+        if (!ok) break;
+        if (elect_one_sync()) {
+            issue_s(sbase % 3u, 0, ks);
+            if (nb == 1) mma_commit(&bars.q_empty[0]);
+        }
+        __syncwarp();
+        ok = warp_wait(&bars.q_full[1], qcnt & 1u, abort_flag, a.timeout_ns);
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one_sync()) {
+            issue_s((sbase + 1u) % 3u, 1, ks);
+            mma_commit(&bars.kv_empty[ks]);
+            if (nb == 1) mma_commit(&bars.q_empty[1]);
+        }
+        __syncwarp();
+        uint32_t ks_next = 0;  // ring slot of K_{j+1}
+        if (nb > 1) {
+            ks_next = wait_pos(kv_base + 2u);
+            if (!ok) break;
+            if (elect_one_sync()) {
+                issue_s((sbase + 2u) % 3u, 0, ks_next);
+                if (nb == 2) mma_commit(&bars.q_empty[0]);
+            }
+            __syncwarp();
+        }
+        for (int j = 0; j < nb && ok; ++j) {
+            const uint32_t k0 = sbase + 2u * j;
+            const uint32_t vs = wait_pos(kv_base + 2u * j + 1u);  // V_j
+            if (!ok) break;
+            wait_p(k0);
+            if (!ok) break;
+            if (elect_one_sync()) {
+                issue_pv(k0 % 3u, 0, vs, j > 0);
+                if (j == nb - 1) mma_commit(&bars.o_full[0]);
+                if (j + 1 < nb) {  // S_1(j+1) into the buffer P_0(j) leaves
+                    issue_s(k0 % 3u, 1, ks_next);
+                    mma_commit(&bars.kv_empty[ks_next]);
+                    if (j + 1 == nb - 1) mma_commit(&bars.q_empty[1]);
+                }
+            }
+            __syncwarp();
+            wait_p(k0 + 1u);
+            if (!ok) break;
+            if (elect_one_sync()) {
+                issue_pv((k0 + 1u) % 3u, 1, vs, j > 0);
+                if (j == nb - 1) mma_commit(&bars.o_full[1]);
+                mma_commit(&bars.kv_empty[vs]);
+            }
+            __syncwarp();
+            if (j + 2 < nb) {  // S_0(j+2) into the buffer P_1(j) leaves
+                ks_next = wait_pos(kv_base + 2u * (j + 2));
+                if (!ok) break;
+                if (elect_one_sync()) {
+                    issue_s((k0 + 1u) % 3u, 0, ks_next);
+                    if (j + 2 == nb - 1) mma_commit(&bars.q_empty[0]);
+                }
+                __syncwarp();
+            }
+        }
+        kv_base += 2u * nb;
+        sbase += 2u * nb;
+        ++qcnt;
+    }
+
+    // Drain: every MMA issued above has completed before TMEM is released.
+    if (elect_one_sync()) mma_commit(bars.drain);
+    __syncwarp();
+    warp_wait(bars.drain, 0u, nullptr, a.timeout_ns);
+}
+
+template <bool BF16, bool CAUSAL>
+__device__ void softmax_role_rot(const TcArgs& a, const Bars& bars, uint32_t tmem_base,
+                                 volatile uint32_t* abort_flag) {
+    constexpr int D = 64;
+    const int warp = threadIdx.x / 32;
+    const int tile = warp / 4;
+    const int trow = threadIdx.x % kTcBM;
+    const uint32_t lane_field = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t tO = tmem_base + lane_field + 3 * kTcBN + tile * D;
+    const float sl2 = a.scale_log2;
+
+    uint32_t scnt0 = 0, scnt1 = 0, scnt2 = 0;  // products of this tile seen in each buffer
+    uint32_t tasks_done = 0;                   // o_full phases
+    uint32_t pv_base = 0;                      // P.V products of this tile in earlier tasks
+    uint32_t sbase = 0;                        // products of both tiles in earlier tasks
+    for (int t = blockIdx.x; t < a.num_tasks; t += gridDim.x) {
+        const Task tk = decode_task<CAUSAL, true>(t, a);
+        const int nb = tk.nbmax;
+        const int row0 = tk.q0 + tile * kTcBM;
+        const int row = row0 + trow;
+        const int lim = CAUSAL ? min(row + 1, a.N) : a.N;  // keys < lim are visible to this row
+
+        float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
+        for (int j = 0; j < nb; ++j) {
+            const uint32_t b = (sbase + 2u * j + tile) % 3u;
+            const uint32_t tS = tmem_base + lane_field + b * kTcBN;
+            const uint32_t use = (b == 0u) ? scnt0 : ((b == 1u) ? scnt1 : scnt2);
+            const bool ok = warp_wait(&bars.s_full[b * 2 + tile], use & 1u, abort_flag, a.timeout_ns);
+            scnt0 += (b == 0u) ? 1u : 0u;
+            scnt1 += (b == 1u) ? 1u : 0u;
+            scnt2 += (b == 2u) ? 1u : 0u;
+            if (!ok) return;
+            tc_fence_after();
+
+            uint32_t sr[kTcBN / 32][32];
+            float cmx[kTcBN / 32];
+#pragma unroll
+            for (int c = 0; c < kTcBN / 32; ++c) tmem_ld32_max(tS + c * 32, sr[c], cmx[c]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < kTcBN / 32; ++c) {
+                reg_fence(sr[c]);
+                reg_fence(cmx[c]);
+            }
+            float s[kTcBN];
+#pragma unroll
+            for (int c = 0; c < kTcBN; ++c) s[c] = __uint_as_float(sr[c / 32][c % 32]);
+
+            const int kb = j * kTcBN;
+            const bool need_mask = (kb + kTcBN > a.N) || (CAUSAL && kb + kTcBN - 1 > row0);
+            float mblk = fmaxf(fmaxf(cmx[0], cmx[1]), fmaxf(cmx[2], cmx[3]));
+            if (need_mask) {
+                const int vis = lim - kb;
+#pragma unroll
+                for (int c = 0; c < kTcBN; ++c)
+                    if (c >= vis) s[c] = -INFINITY;
+                float mx[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) mx[u] = s[u];
+#pragma unroll
+                for (int c = 8; c < kTcBN; c += 2)
+                    mx[(c / 2) % 8] = fmax3f(mx[(c / 2) % 8], s[c], s[c + 1]);
+                mblk = fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]),
+                              fmaxf(mx[6], mx[7]));
+            }
+            const float m_new = fmaxf(m_run, mblk * sl2);
+
+            if (j == 0) {
+                m_run = m_new;
+            } else {
+                const bool grow = (m_new - m_run) > kRescaleThreshold;
+                if (__any_sync(0xffffffffu, grow)) {
+                    // O_i holds P.V_i(j-1) only once that product is done.
+                    if (!warp_wait(&bars.o_ready[tile], (pv_base + j - 1) & 1u, abort_flag,
+                                   a.timeout_ns))
+                        return;
+                    tc_fence_after();
+                    const float alpha = ex2_approx(m_run - m_new);
+                    l_run *= alpha;
+                    l_exact *= alpha;
+                    m_run = m_new;
+                    uint32_t r[32];
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        tmem_ld32(tO + c * 32, r);
+                        tmem_wait_ld();
+                        reg_fence(r);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                        tmem_st32(tO + c * 32, r);
+                    }
+                }
+            }
+            const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+
+#pragma unroll
+            for (int c = 0; c < kTcBN / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float x0, x1;
+                    ffma2(x0, x1, s[c * 32 + 2 * e], s[c * 32 + 2 * e + 1], sl2, sl2, neg_m, neg_m);
+                    s[c * 32 + 2 * e] = ex2_approx(x0);
+                    s[c * 32 + 2 * e + 1] = ex2_approx(x1);
+                    pk[e] = pack2(s[c * 32 + 2 * e], s[c * 32 + 2 * e + 1], BF16);
+                }
+                tmem_st16(tS + c * 16, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if ((threadIdx.x % 32) == 0) mbar_arrive(&bars.p_full[b]);
+            float la[8], le[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                la[u] = 0.f;
+                le[u] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < kTcBN / 2; ++e) {
+                add_packed16_to_f32<BF16>(la[(e % 4) * 2], la[(e % 4) * 2 + 1],
+                                          pack2(s[2 * e], s[2 * e + 1], BF16));
+                fadd2(le[(e % 4) * 2], le[(e % 4) * 2 + 1], s[2 * e], s[2 * e + 1]);
+            }
+            l_run += ((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7]));
+            l_exact += ((le[0] + le[1]) + (le[2] + le[3])) + ((le[4] + le[5]) + (le[6] + le[7]));
+        }
+
+        // Epilogue: O = O~ / l, LSE = (m + log2 l) ln 2, rows < N only.
+        const bool ok = warp_wait(&bars.o_full[tile], tasks_done & 1u, abort_flag, a.timeout_ns);
+        ++tasks_done;
+        if (!ok) return;
+        tc_fence_after();
+        const float inv_l = 1.f / l_run;
+        const bool valid = row < a.N;
+        uint8_t* orow = reinterpret_cast<uint8_t*>(a.o) +
+                        ((static_cast<int64_t>(tk.bh) * a.N + row) * D) * 2;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tO + c * 32, r);
+            tmem_wait_ld();
+            reg_fence(r);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                pk[e] = pack2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l,
+                              BF16);
+            if (valid) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                    dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+            }
+        }
+        if (valid && a.lse != nullptr)
+            a.lse[static_cast<int64_t>(tk.bh) * a.N + row] = (m_run + log2f(l_exact)) * kLn2;
+        tc_fence_before();
+        pv_base += static_cast<uint32_t>(nb);
+        sbase += 2u * nb;
+    }
+}
+
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ TcArgs a) {
     using L = TcLayout<D>;
@@ -577,10 +897,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.q_full[i], 1);
             mbar_init(&bars.q_empty[i], 1);
-            mbar_init(&bars.s_full[i], 1);
-            mbar_init(&bars.p_full[i], kTcBM / 32);  // one arrival per softmax warp
             mbar_init(&bars.o_full[i], 1);
+            if (L::kRot) mbar_init(&bars.o_ready[i], 1);
         }
+        for (int b = 0; b < L::kSFull; ++b) mbar_init(&bars.s_full[b], 1);
+        for (int b = 0; b < L::kPFull; ++b)
+            mbar_init(&bars.p_full[b], kTcBM / 32);  // one arrival per softmax warp
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(&bars.kv_full[s], 1);
             mbar_init(&bars.kv_empty[s], 1);
@@ -605,13 +927,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid
 
     if (warp < 8) {
         regs_increase<kSoftmaxRegs>();
-        softmax_role<D, BF16, CAUSAL>(a, bars, tmem_base, abort_flag);
+        if constexpr (L::kRot)
+            softmax_role_rot<BF16, CAUSAL>(a, bars, tmem_base, abort_flag);
+        else
+            softmax_role<D, BF16, CAUSAL>(a, bars, tmem_base, abort_flag);
     } else {
         regs_decrease<kControlRegs>();
-        if (warp == 8)
-            mma_role<D, BF16, CAUSAL>(a, smem, bars, tmem_base, abort_flag);
-        else if (warp == 9)
+        if (warp == 8) {
+            if constexpr (L::kRot)
+                mma_role_rot<BF16, CAUSAL>(a, smem, bars, tmem_base, abort_flag);
+            else
+                mma_role<D, BF16, CAUSAL>(a, smem, bars, tmem_base, abort_flag);
+        } else if (warp == 9) {
             producer_role<D, CAUSAL>(a, smem, bars, abort_flag);
+        }
     }
     __syncwarp();
     tc_fence_before();
