@@ -496,19 +496,23 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
             // P = exp2(s*scale*log2e - m) rounded to the operand type, written
             // over the first half of S.  l_run sums exactly the rounded values
             // the P.V product consumes, so O is normalised by the weights it
-            // was built from; l_exact sums the unrounded ones for the LSE.
+            // was built from; l_exact sums the unrounded ones for the LSE (on
+            // the way; l_run after the hand-off).
+            uint32_t pk[kTcBN / 32][16];
+            float le[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) le[u] = 0.f;
 #pragma unroll
             for (int c = 0; c < kTcBN / 32; ++c) {
-                uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     float x0, x1;
                     ffma2(x0, x1, s[c * 32 + 2 * e], s[c * 32 + 2 * e + 1], sl2, sl2, neg_m, neg_m);
-                    s[c * 32 + 2 * e] = ex2_approx(x0);
-                    s[c * 32 + 2 * e + 1] = ex2_approx(x1);
-                    pk[e] = pack2(s[c * 32 + 2 * e], s[c * 32 + 2 * e + 1], BF16);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    pk[c][e] = pack2(p0, p1, BF16);
+                    fadd2(le[(e % 4) * 2], le[(e % 4) * 2 + 1], p0, p1);
                 }
-                tmem_st16(tS + c * 16, pk);
+                tmem_st16(tS + c * 16, pk[c]);
             }
             // P stored: hand it to the MMA warp (one arrival per warp, after
             // every lane's stores have completed).
@@ -516,21 +520,16 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
             tc_fence_before();
             __syncwarp();
             if ((threadIdx.x % 32) == 0) mbar_arrive(&bars.p_full[tile]);
-            // The row sums feed nothing the MMA warp waits for, so they are
-            // formed after the hand-off (the 16-bit values rounded again, as
-            // the P.V product consumed them).
-            float la[8], le[8];
+            // The sum of the rounded P (which normalises O) feeds nothing the
+            // MMA warp waits for, so it is formed after the hand-off.
+            float la[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                la[u] = 0.f;
-                le[u] = 0.f;
-            }
+            for (int u = 0; u < 8; ++u) la[u] = 0.f;
 #pragma unroll
-            for (int e = 0; e < kTcBN / 2; ++e) {
-                add_packed16_to_f32<BF16>(la[(e % 4) * 2], la[(e % 4) * 2 + 1],
-                                          pack2(s[2 * e], s[2 * e + 1], BF16));
-                fadd2(le[(e % 4) * 2], le[(e % 4) * 2 + 1], s[2 * e], s[2 * e + 1]);
-            }
+            for (int c = 0; c < kTcBN / 32; ++c)
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    add_packed16_to_f32<BF16>(la[(e % 4) * 2], la[(e % 4) * 2 + 1], pk[c][e]);
             l_run += ((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7]));
             l_exact += ((le[0] + le[1]) + (le[2] + le[3])) + ((le[4] + le[5]) + (le[6] + le[7]));
         }
@@ -807,35 +806,39 @@ __device__ void softmax_role_rot(const TcArgs& a, const Bars& bars, uint32_t tme
             }
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
 
+            // P = exp2(s*scale*log2e - m) rounded to the operand type, written
+            // over the first half of S; l_exact sums the unrounded values (for
+            // the LSE) on the way.
+            uint32_t pk[kTcBN / 32][16];
+            float le[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) le[u] = 0.f;
 #pragma unroll
             for (int c = 0; c < kTcBN / 32; ++c) {
-                uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     float x0, x1;
                     ffma2(x0, x1, s[c * 32 + 2 * e], s[c * 32 + 2 * e + 1], sl2, sl2, neg_m, neg_m);
-                    s[c * 32 + 2 * e] = ex2_approx(x0);
-                    s[c * 32 + 2 * e + 1] = ex2_approx(x1);
-                    pk[e] = pack2(s[c * 32 + 2 * e], s[c * 32 + 2 * e + 1], BF16);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    pk[c][e] = pack2(p0, p1, BF16);
+                    fadd2(le[(e % 4) * 2], le[(e % 4) * 2 + 1], p0, p1);
                 }
-                tmem_st16(tS + c * 16, pk);
+                tmem_st16(tS + c * 16, pk[c]);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if ((threadIdx.x % 32) == 0) mbar_arrive(&bars.p_full[b]);
-            float la[8], le[8];
+            // The sum of the rounded P (which normalises O) feeds nothing the
+            // MMA warp waits for, so it is formed after the hand-off.
+            float la[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                la[u] = 0.f;
-                le[u] = 0.f;
-            }
+            for (int u = 0; u < 8; ++u) la[u] = 0.f;
 #pragma unroll
-            for (int e = 0; e < kTcBN / 2; ++e) {
-                add_packed16_to_f32<BF16>(la[(e % 4) * 2], la[(e % 4) * 2 + 1],
-                                          pack2(s[2 * e], s[2 * e + 1], BF16));
-                fadd2(le[(e % 4) * 2], le[(e % 4) * 2 + 1], s[2 * e], s[2 * e + 1]);
-            }
+            for (int c = 0; c < kTcBN / 32; ++c)
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    add_packed16_to_f32<BF16>(la[(e % 4) * 2], la[(e % 4) * 2 + 1], pk[c][e]);
             l_run += ((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7]));
             l_exact += ((le[0] + le[1]) + (le[2] + le[3])) + ((le[4] + le[5]) + (le[6] + le[7]));
         }
