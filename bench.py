@@ -67,9 +67,9 @@ BWD_FLOP_FACTOR = 2.5
 # once the kernel has changed.
 KERNEL_SOURCES = {"tc": ["fwd_tc.cu", "sm103_ptx.cuh"], "ffma": ["fwd_ffma.cu"]}
 NCU_TRAFFIC = {
-    "bf16_B4_H16_N4096_D128": (201410048 + 36410112, "ee8bc61f5b17fde5"),
-    "bf16_B2_H32_N8192_D128_causal_qstd4": (2624888320 + 126341120, "ee8bc61f5b17fde5"),
-    "fp16_B1_H16_N16000_D64_causal": (126827776 + 13759744, "ee8bc61f5b17fde5"),
+    "bf16_B4_H16_N4096_D128": (201595392 + 36544768, "eb150c763abf0c84"),
+    "bf16_B2_H32_N8192_D128_causal_qstd4": (2465548800 + 128443136, "eb150c763abf0c84"),
+    "fp16_B1_H16_N16000_D64_causal": (132226816 + 14801920, "eb150c763abf0c84"),
     "fp32_B4_H8_N8192_D64_causal": (201690624 + 51116544, "224b5f7dc90ca5e2"),
 }
 

@@ -36,6 +36,11 @@
 // and vice versa.  A commit after S_i(j+1) fires only once PV_i(j) is done,
 // which is what lets the softmax warpgroup rescale O_i right after it sees
 // S_i(j+1).
+//
+// That is the D = 128 layout.  At D = 64 the TMEM has room for a third S
+// buffer, and the two tiles rotate through three buffers so that a tile's
+// next scores are computed while its softmax still works on the current
+// ones (mma_role_rot / softmax_role_rot below).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
