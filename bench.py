@@ -70,7 +70,7 @@ NCU_TRAFFIC = {
     "bf16_B4_H16_N4096_D128": (201595392 + 36544768, "eb150c763abf0c84"),
     "bf16_B2_H32_N8192_D128_causal_qstd4": (2465548800 + 128443136, "eb150c763abf0c84"),
     "fp16_B1_H16_N16000_D64_causal": (132226816 + 14801920, "eb150c763abf0c84"),
-    "fp32_B4_H8_N8192_D64_causal": (201690624 + 51116544, "224b5f7dc90ca5e2"),
+    "fp32_B4_H8_N8192_D64_causal": (201679616 + 50925056, "e5b4a15b206c290b"),
 }
 
 

@@ -10,8 +10,8 @@
 //   * attn_fwd_ffma_tiled_kernel (fattn_fwd, fp32): 256 threads share the
 //     128 x BC score tile and the 128 x D output tile as 8-row register
 //     micro-tiles, so one 16-byte shared-memory read feeds about 11 FMAs at
-//     D = 64; P passes through shared memory to the lanes that own the same
-//     rows;
+//     D = 64, issued as packed fp32x2 FMAs; P passes through shared memory
+//     to the lanes that own the same rows;
 //   * attn_fwd_ffma_row_kernel (fattn_fwd_f32_rowwise): the page's one query
 //     row per thread, where a read feeds 4 FMAs, which caps the FP32 pipe
 //     near 40 % on this part.
@@ -33,6 +33,20 @@ __device__ __forceinline__ float ex2f(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1) in one packed fp32 FMA instruction:
+// two FMAs per issue slot.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, bool valid) {
@@ -355,12 +369,17 @@ __global__ void __launch_bounds__(kTiledThreads, MIN_BLOCKS)
         const float* Vt = Vs + cur * L::kKVFloats;
         const int kb = j * BC;
 
-        // S micro-tile: rows rg + 16 i, keys cg + 16 c.
-        float s[kTiledRows][L::kKeys];
+        // S micro-tile: rows rg + 16 i, keys cg + 16 c.  Even and odd
+        // features accumulate in the two halves of packed FMAs and are added
+        // at the end.
+        float s[kTiledRows][L::kKeys], so[kTiledRows][L::kKeys];
 #pragma unroll
         for (int i = 0; i < kTiledRows; ++i)
 #pragma unroll
-            for (int c = 0; c < L::kKeys; ++c) s[i][c] = 0.f;
+            for (int c = 0; c < L::kKeys; ++c) {
+                s[i][c] = 0.f;
+                so[i][c] = 0.f;
+            }
 #pragma unroll
         for (int d4 = 0; d4 < D / 4; ++d4) {
             float4 qf[kTiledRows], kf[L::kKeys];
@@ -374,12 +393,14 @@ __global__ void __launch_bounds__(kTiledThreads, MIN_BLOCKS)
             for (int i = 0; i < kTiledRows; ++i)
 #pragma unroll
                 for (int c = 0; c < L::kKeys; ++c) {
-                    s[i][c] = fmaf(qf[i].x, kf[c].x, s[i][c]);
-                    s[i][c] = fmaf(qf[i].y, kf[c].y, s[i][c]);
-                    s[i][c] = fmaf(qf[i].z, kf[c].z, s[i][c]);
-                    s[i][c] = fmaf(qf[i].w, kf[c].w, s[i][c]);
+                    fma2(s[i][c], so[i][c], qf[i].x, qf[i].y, kf[c].x, kf[c].y, s[i][c], so[i][c]);
+                    fma2(s[i][c], so[i][c], qf[i].z, qf[i].w, kf[c].z, kf[c].w, s[i][c], so[i][c]);
                 }
         }
+#pragma unroll
+        for (int i = 0; i < kTiledRows; ++i)
+#pragma unroll
+            for (int c = 0; c < L::kKeys; ++c) s[i][c] += so[i][c];
 
         // Online softmax per row (single-correction form), P over the row's
         // 16 owners; keys past N and (causal) past the row are masked.
@@ -436,10 +457,10 @@ __global__ void __launch_bounds__(kTiledThreads, MIN_BLOCKS)
                 const float4 vf = *reinterpret_cast<const float4*>(Vt + key * L::kStride + u * 64 + cg * 4);
 #pragma unroll
                 for (int i = 0; i < kTiledRows; ++i) {
-                    acc[i][u * 4 + 0] = fmaf(p[i], vf.x, acc[i][u * 4 + 0]);
-                    acc[i][u * 4 + 1] = fmaf(p[i], vf.y, acc[i][u * 4 + 1]);
-                    acc[i][u * 4 + 2] = fmaf(p[i], vf.z, acc[i][u * 4 + 2]);
-                    acc[i][u * 4 + 3] = fmaf(p[i], vf.w, acc[i][u * 4 + 3]);
+                    fma2(acc[i][u * 4 + 0], acc[i][u * 4 + 1], p[i], p[i], vf.x, vf.y,
+                         acc[i][u * 4 + 0], acc[i][u * 4 + 1]);
+                    fma2(acc[i][u * 4 + 2], acc[i][u * 4 + 3], p[i], p[i], vf.z, vf.w,
+                         acc[i][u * 4 + 2], acc[i][u * 4 + 3]);
                 }
             }
         }
