@@ -40,7 +40,7 @@
 // That is the D = 128 layout.  At D = 64 the TMEM has room for a third S
 // buffer, and the two tiles rotate through three buffers so that a tile's
 // next scores are computed while its softmax still works on the current
-// ones (mma_role_rot / softmax_role_rot below).
+// ones (mma_role_rot below; softmax_role serves both layouts).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -403,175 +403,6 @@ __device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint3
 // ---------------------------------------------------------------------------
 // Softmax + correction + epilogue (one warpgroup per Q tile)
 // ---------------------------------------------------------------------------
-template <int D, bool BF16, bool CAUSAL>
-__device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_base,
-                             volatile uint32_t* abort_flag) {
-    const int warp = threadIdx.x / 32;
-    const int tile = warp / 4;                  // which Q tile / S, P, O buffer
-    const int trow = threadIdx.x % kTcBM;       // row within the tile == TMEM lane
-    const uint32_t lane_field = static_cast<uint32_t>((warp % 4) * 32) << 16;
-    const uint32_t tS = tmem_base + lane_field + tile * kTcBN;
-    const uint32_t tO = tmem_base + lane_field + 2 * kTcBN + tile * D;
-    const float sl2 = a.scale_log2;
-
-    uint32_t scnt = 0, ocnt = 0;
-    for (int t = blockIdx.x; t < a.num_tasks; t += gridDim.x) {
-        const Task tk = decode_task<CAUSAL>(t, a);
-        const int nb = tk.nb[tile];
-        if (nb == 0) continue;
-        const int row0 = tk.q0 + tile * kTcBM;
-        const int row = row0 + trow;
-        const int lim = CAUSAL ? min(row + 1, a.N) : a.N;  // keys < lim are visible to this row
-
-        float m_run = -INFINITY;  // running max of scale*log2(e)*s
-        float l_run = 0.f;        // running sum of the 16-bit P values fed to the MMA (normalises O)
-        float l_exact = 0.f;      // running sum of the unrounded P values (gives the LSE)
-
-        for (int j = 0; j < nb; ++j) {
-            const bool ok = warp_wait(&bars.s_full[tile], scnt & 1u, abort_flag, a.timeout_ns);
-            ++scnt;
-            if (!ok) return;
-            tc_fence_after();
-
-            // The whole score row: four 32-column loads in flight, one wait.
-            // The loads also reduce: cmx[c] = max of the 32 scores of chunk c
-            // (tcgen05.ld.red), the row max of every tile without masked keys.
-            uint32_t sr[kTcBN / 32][32];
-            float cmx[kTcBN / 32];
-#pragma unroll
-            for (int c = 0; c < kTcBN / 32; ++c) tmem_ld32_max(tS + c * 32, sr[c], cmx[c]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < kTcBN / 32; ++c) {
-                reg_fence(sr[c]);
-                reg_fence(cmx[c]);
-            }
-            float s[kTcBN];
-#pragma unroll
-            for (int c = 0; c < kTcBN; ++c) s[c] = __uint_as_float(sr[c / 32][c % 32]);
-
-            const int kb = j * kTcBN;
-            const bool need_mask = (kb + kTcBN > a.N) || (CAUSAL && kb + kTcBN - 1 > row0);
-            float mblk = fmaxf(fmaxf(cmx[0], cmx[1]), fmaxf(cmx[2], cmx[3]));
-            if (need_mask) {
-                // Keys past N or past the row: masked here, and the row max
-                // taken over the visible scores only.
-                const int vis = lim - kb;
-#pragma unroll
-                for (int c = 0; c < kTcBN; ++c)
-                    if (c >= vis) s[c] = -INFINITY;
-                float mx[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) mx[u] = s[u];
-#pragma unroll
-                for (int c = 8; c < kTcBN; c += 2)
-                    mx[(c / 2) % 8] = fmax3f(mx[(c / 2) % 8], s[c], s[c + 1]);
-                mblk = fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]),
-                              fmaxf(mx[6], mx[7]));
-            }
-            const float m_new = fmaxf(m_run, mblk * sl2);
-
-            if (j == 0) {
-                m_run = m_new;
-            } else {
-                // Rescale O and l only when some row of the warp saw its max
-                // rise by more than the threshold; otherwise keep the stale
-                // max for P and l alike (exact in exact arithmetic, P <= 2^8).
-                const bool grow = (m_new - m_run) > kRescaleThreshold;
-                if (__any_sync(0xffffffffu, grow)) {
-                    const float alpha = ex2_approx(m_run - m_new);
-                    l_run *= alpha;
-                    l_exact *= alpha;
-                    m_run = m_new;
-                    uint32_t r[32];
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        tmem_ld32(tO + c * 32, r);
-                        tmem_wait_ld();
-                        reg_fence(r);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                        tmem_st32(tO + c * 32, r);
-                    }
-                }
-            }
-            const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-
-            // P = exp2(s*scale*log2e - m) rounded to the operand type, written
-            // over the first half of S.  l_run sums exactly the rounded values
-            // the P.V product consumes, so O is normalised by the weights it
-            // was built from; l_exact sums the unrounded ones for the LSE (on
-            // the way; l_run after the hand-off).
-            uint32_t pk[kTcBN / 32][16];
-            float le[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) le[u] = 0.f;
-#pragma unroll
-            for (int c = 0; c < kTcBN / 32; ++c) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float x0, x1;
-                    ffma2(x0, x1, s[c * 32 + 2 * e], s[c * 32 + 2 * e + 1], sl2, sl2, neg_m, neg_m);
-                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                    pk[c][e] = pack2(p0, p1, BF16);
-                    fadd2(le[(e % 4) * 2], le[(e % 4) * 2 + 1], p0, p1);
-                }
-                tmem_st16(tS + c * 16, pk[c]);
-            }
-            // P stored: hand it to the MMA warp (one arrival per warp, after
-            // every lane's stores have completed).
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if ((threadIdx.x % 32) == 0) mbar_arrive(&bars.p_full[tile]);
-            // The sum of the rounded P (which normalises O) feeds nothing the
-            // MMA warp waits for, so it is formed after the hand-off.
-            float la[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) la[u] = 0.f;
-#pragma unroll
-            for (int c = 0; c < kTcBN / 32; ++c)
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    add_packed16_to_f32<BF16>(la[(e % 4) * 2], la[(e % 4) * 2 + 1], pk[c][e]);
-            l_run += ((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7]));
-            l_exact += ((le[0] + le[1]) + (le[2] + le[3])) + ((le[4] + le[5]) + (le[6] + le[7]));
-        }
-
-        // Epilogue: O = O~ / l, LSE = (m + log2 l) ln 2, rows < N only.
-        const bool ok = warp_wait(&bars.o_full[tile], ocnt & 1u, abort_flag, a.timeout_ns);
-        ++ocnt;
-        if (!ok) return;
-        tc_fence_after();
-        const float inv_l = 1.f / l_run;
-        const bool valid = row < a.N;
-        uint8_t* orow = reinterpret_cast<uint8_t*>(a.o) +
-                        ((static_cast<int64_t>(tk.bh) * a.N + row) * D) * 2;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tO + c * 32, r);
-            tmem_wait_ld();
-            reg_fence(r);
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                pk[e] = pack2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l,
-                              BF16);
-            if (valid) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
-#pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4)
-                    dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-            }
-        }
-        if (valid && a.lse != nullptr)
-            a.lse[static_cast<int64_t>(tk.bh) * a.N + row] = (m_run + log2f(l_exact)) * kLn2;
-        tc_fence_before();
-    }
-}
-
 // ---------------------------------------------------------------------------
 // D = 64: three S buffers shared by the two Q tiles
 // ---------------------------------------------------------------------------
@@ -715,40 +546,61 @@ __device__ void mma_role_rot(const TcArgs& a, uint8_t* smem, const Bars& bars, u
     warp_wait(bars.drain, 0u, nullptr, a.timeout_ns);
 }
 
-template <bool BF16, bool CAUSAL>
-__device__ void softmax_role_rot(const TcArgs& a, const Bars& bars, uint32_t tmem_base,
-                                 volatile uint32_t* abort_flag) {
-    constexpr int D = 64;
+// ---------------------------------------------------------------------------
+// Softmax + correction + epilogue (one warpgroup per Q tile), both layouts
+// ---------------------------------------------------------------------------
+template <int D, bool BF16, bool CAUSAL>
+__device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_base,
+                             volatile uint32_t* abort_flag) {
+    constexpr bool kRot = TcLayout<D>::kRot;  // D = 64: three rotating S buffers
     const int warp = threadIdx.x / 32;
-    const int tile = warp / 4;
-    const int trow = threadIdx.x % kTcBM;
+    const int tile = warp / 4;                  // which Q tile / O accumulator
+    const int trow = threadIdx.x % kTcBM;       // row within the tile == TMEM lane
     const uint32_t lane_field = static_cast<uint32_t>((warp % 4) * 32) << 16;
-    const uint32_t tO = tmem_base + lane_field + 3 * kTcBN + tile * D;
+    const uint32_t tO = tmem_base + lane_field + (kRot ? 3 : 2) * kTcBN + tile * D;
     const float sl2 = a.scale_log2;
 
-    uint32_t scnt0 = 0, scnt1 = 0, scnt2 = 0;  // products of this tile seen in each buffer
-    uint32_t tasks_done = 0;                   // o_full phases
-    uint32_t pv_base = 0;                      // P.V products of this tile in earlier tasks
-    uint32_t sbase = 0;                        // products of both tiles in earlier tasks
+    // Barrier phases: D = 128 counts the S products of this tile on
+    // s_full[tile]; D = 64 counts them per buffer on s_full[b * 2 + tile].
+    uint32_t scnt0 = 0, scnt1 = 0, scnt2 = 0;
+    uint32_t ocnt = 0;     // tasks of this tile (o_full phases)
+    uint32_t pv_base = 0;  // D = 64: P.V products of this tile in earlier tasks
+    uint32_t sbase = 0;    // D = 64: S products of both tiles in earlier tasks
     for (int t = blockIdx.x; t < a.num_tasks; t += gridDim.x) {
-        const Task tk = decode_task<CAUSAL, true>(t, a);
-        const int nb = tk.nbmax;
+        const Task tk = decode_task<CAUSAL, kRot>(t, a);
+        const int nb = tk.nb[tile];
+        if constexpr (!kRot) {
+            if (nb == 0) continue;  // tile past N (the three-buffer layout computes it anyway)
+        }
         const int row0 = tk.q0 + tile * kTcBM;
         const int row = row0 + trow;
         const int lim = CAUSAL ? min(row + 1, a.N) : a.N;  // keys < lim are visible to this row
 
-        float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
+        float m_run = -INFINITY;  // running max of scale*log2(e)*s
+        float l_run = 0.f;        // running sum of the 16-bit P values fed to the MMA (normalises O)
+        float l_exact = 0.f;      // running sum of the unrounded P values (gives the LSE)
+
         for (int j = 0; j < nb; ++j) {
-            const uint32_t b = (sbase + 2u * j + tile) % 3u;
+            uint32_t b, use;
+            if constexpr (kRot) {
+                b = (sbase + 2u * j + tile) % 3u;
+                use = (b == 0u) ? scnt0 : ((b == 1u) ? scnt1 : scnt2);
+                scnt0 += (b == 0u) ? 1u : 0u;
+                scnt1 += (b == 1u) ? 1u : 0u;
+                scnt2 += (b == 2u) ? 1u : 0u;
+            } else {
+                b = static_cast<uint32_t>(tile);
+                use = scnt0++;
+            }
             const uint32_t tS = tmem_base + lane_field + b * kTcBN;
-            const uint32_t use = (b == 0u) ? scnt0 : ((b == 1u) ? scnt1 : scnt2);
-            const bool ok = warp_wait(&bars.s_full[b * 2 + tile], use & 1u, abort_flag, a.timeout_ns);
-            scnt0 += (b == 0u) ? 1u : 0u;
-            scnt1 += (b == 1u) ? 1u : 0u;
-            scnt2 += (b == 2u) ? 1u : 0u;
+            const bool ok = warp_wait(&bars.s_full[kRot ? b * 2 + tile : b], use & 1u, abort_flag,
+                                      a.timeout_ns);
             if (!ok) return;
             tc_fence_after();
 
+            // The whole score row: four 32-column loads in flight, one wait.
+            // The loads also reduce: cmx[c] = max of the 32 scores of chunk c
+            // (tcgen05.ld.red), the row max of every tile without masked keys.
             uint32_t sr[kTcBN / 32][32];
             float cmx[kTcBN / 32];
 #pragma unroll
@@ -767,6 +619,8 @@ __device__ void softmax_role_rot(const TcArgs& a, const Bars& bars, uint32_t tme
             const bool need_mask = (kb + kTcBN > a.N) || (CAUSAL && kb + kTcBN - 1 > row0);
             float mblk = fmaxf(fmaxf(cmx[0], cmx[1]), fmaxf(cmx[2], cmx[3]));
             if (need_mask) {
+                // Keys past N or past the row: masked here, and the row max
+                // taken over the visible scores only.
                 const int vis = lim - kb;
 #pragma unroll
                 for (int c = 0; c < kTcBN; ++c)
@@ -785,13 +639,19 @@ __device__ void softmax_role_rot(const TcArgs& a, const Bars& bars, uint32_t tme
             if (j == 0) {
                 m_run = m_new;
             } else {
+                // Rescale O and l only when some row of the warp saw its max
+                // rise by more than the threshold; otherwise keep the stale
+                // max for P and l alike (exact in exact arithmetic, P <= 2^8).
                 const bool grow = (m_new - m_run) > kRescaleThreshold;
                 if (__any_sync(0xffffffffu, grow)) {
-                    // O_i holds P.V_i(j-1) only once that product is done.
-                    if (!warp_wait(&bars.o_ready[tile], (pv_base + j - 1) & 1u, abort_flag,
-                                   a.timeout_ns))
-                        return;
-                    tc_fence_after();
+                    if (kRot) {
+                        // O_i holds P.V_i(j-1) only once that product is done
+                        // (at D = 128 the commit of S_i(j) already implies it).
+                        if (!warp_wait(&bars.o_ready[tile], (pv_base + j - 1) & 1u, abort_flag,
+                                       a.timeout_ns))
+                            return;
+                        tc_fence_after();
+                    }
                     const float alpha = ex2_approx(m_run - m_new);
                     l_run *= alpha;
                     l_exact *= alpha;
@@ -812,8 +672,10 @@ __device__ void softmax_role_rot(const TcArgs& a, const Bars& bars, uint32_t tme
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
 
             // P = exp2(s*scale*log2e - m) rounded to the operand type, written
-            // over the first half of S; l_exact sums the unrounded values (for
-            // the LSE) on the way.
+            // over the first half of S.  l_run sums exactly the rounded values
+            // the P.V product consumes, so O is normalised by the weights it
+            // was built from; l_exact sums the unrounded ones for the LSE (on
+            // the way; l_run after the hand-off).
             uint32_t pk[kTcBN / 32][16];
             float le[8];
 #pragma unroll
@@ -830,6 +692,8 @@ __device__ void softmax_role_rot(const TcArgs& a, const Bars& bars, uint32_t tme
                 }
                 tmem_st16(tS + c * 16, pk[c]);
             }
+            // P stored: hand it to the MMA warp (one arrival per warp, after
+            // every lane's stores have completed).
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -849,8 +713,8 @@ __device__ void softmax_role_rot(const TcArgs& a, const Bars& bars, uint32_t tme
         }
 
         // Epilogue: O = O~ / l, LSE = (m + log2 l) ln 2, rows < N only.
-        const bool ok = warp_wait(&bars.o_full[tile], tasks_done & 1u, abort_flag, a.timeout_ns);
-        ++tasks_done;
+        const bool ok = warp_wait(&bars.o_full[tile], ocnt & 1u, abort_flag, a.timeout_ns);
+        ++ocnt;
         if (!ok) return;
         tc_fence_after();
         const float inv_l = 1.f / l_run;
@@ -878,8 +742,10 @@ __device__ void softmax_role_rot(const TcArgs& a, const Bars& bars, uint32_t tme
         if (valid && a.lse != nullptr)
             a.lse[static_cast<int64_t>(tk.bh) * a.N + row] = (m_run + log2f(l_exact)) * kLn2;
         tc_fence_before();
-        pv_base += static_cast<uint32_t>(nb);
-        sbase += 2u * nb;
+        if constexpr (kRot) {
+            pv_base += static_cast<uint32_t>(nb);
+            sbase += static_cast<uint32_t>(tk.nb[0] + tk.nb[1]);
+        }
     }
 }
 
@@ -935,10 +801,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid
 
     if (warp < 8) {
         regs_increase<kSoftmaxRegs>();
-        if constexpr (L::kRot)
-            softmax_role_rot<BF16, CAUSAL>(a, bars, tmem_base, abort_flag);
-        else
-            softmax_role<D, BF16, CAUSAL>(a, bars, tmem_base, abort_flag);
+        softmax_role<D, BF16, CAUSAL>(a, bars, tmem_base, abort_flag);
     } else {
         regs_decrease<kControlRegs>();
         if (warp == 8) {
