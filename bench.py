@@ -67,9 +67,9 @@ BWD_FLOP_FACTOR = 2.5
 # once the kernel has changed.
 KERNEL_SOURCES = {"tc": ["fwd_tc.cu", "sm103_ptx.cuh"], "ffma": ["fwd_ffma.cu"]}
 NCU_TRAFFIC = {
-    "bf16_B4_H16_N4096_D128": (201595392 + 36544768, "eb150c763abf0c84"),
-    "bf16_B2_H32_N8192_D128_causal_qstd4": (2465548800 + 128443136, "eb150c763abf0c84"),
-    "fp16_B1_H16_N16000_D64_causal": (132226816 + 14801920, "eb150c763abf0c84"),
+    "bf16_B4_H16_N4096_D128": (201401344 + 37754624, "0ad671d8eedf986a"),
+    "bf16_B2_H32_N8192_D128_causal_qstd4": (2534908928 + 127398912, "0ad671d8eedf986a"),
+    "fp16_B1_H16_N16000_D64_causal": (131074304 + 14406400, "0ad671d8eedf986a"),
     "fp32_B4_H8_N8192_D64_causal": (201679616 + 50925056, "e5b4a15b206c290b"),
 }
 
