@@ -65,12 +65,21 @@ BWD_FLOP_FACTOR = 2.5
 # profiles/), tagged with the hash of that kernel's device sources when it
 # was taken.  Reported only while those sources still hash the same; null
 # once the kernel has changed.
-KERNEL_SOURCES = {"tc": ["fwd_tc.cu", "sm103_ptx.cuh"], "ffma": ["fwd_ffma.cu"]}
+KERNEL_SOURCES = {"tc": ["fwd_tc.cu", "sm103_ptx.cuh"], "ffma": ["fwd_ffma.cu"],
+                  "unfused": ["fwd_unfused.cu", "sm103_ptx.cuh"]}
 NCU_TRAFFIC = {
     "bf16_B4_H16_N4096_D128": (201401344 + 37754624, "0ad671d8eedf986a"),
     "bf16_B2_H32_N8192_D128_causal_qstd4": (2534908928 + 127398912, "0ad671d8eedf986a"),
     "fp16_B1_H16_N16000_D64_causal": (131074304 + 14406400, "0ad671d8eedf986a"),
     "fp32_B4_H8_N8192_D64_causal": (201679616 + 50925056, "e5b4a15b206c290b"),
+}
+
+
+# The materialising comparator: DRAM bytes of one step (its three kernels).
+NCU_TRAFFIC_UNFUSED = {
+    "bf16_B4_H16_N4096_D128": (6654303488 + 6404445952, "eea14f381a5e072c"),
+    "bf16_B2_H32_N8192_D128_causal_qstd4": (13389511424 + 13121869568, "eea14f381a5e072c"),
+    "fp16_B1_H16_N16000_D64_causal": (12438579200 + 12321152000, "eea14f381a5e072c"),
 }
 
 
@@ -88,9 +97,9 @@ def kernel_source_hash(family):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(w):
-    entry = NCU_TRAFFIC.get(w.name)
-    if entry is None or entry[1] != kernel_source_hash(kernel_family(w)):
+def ncu_traffic(w, unfused=False):
+    entry = (NCU_TRAFFIC_UNFUSED if unfused else NCU_TRAFFIC).get(w.name)
+    if entry is None or entry[1] != kernel_source_hash("unfused" if unfused else kernel_family(w)):
         return None
     return entry[0]
 
@@ -354,7 +363,8 @@ def run_ours(args, w, ws, rank, local):
         gbs = unfused_bytes(w) / (ms_per_step * 1e-3) / 1e9
         peak = float(peaks["hbm_gbs"])
         roof = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                "traffic": None, "scope": "the whole three-kernel step (S, softmax, P V)",
+                "traffic": ncu_traffic(w, unfused=True),
+                "scope": "the whole three-kernel step (S, softmax, P V)",
                 "peak_source": "hbm_gbs (STREAM-style copy) of %s" % peak_src,
                 "algorithmic_bytes": unfused_bytes(w),
                 "tensor_tflops": achieved}
@@ -371,7 +381,8 @@ def run_ours(args, w, ws, rank, local):
                 "peak_source": "%s dense bf16 (cuBLAS burst) of %s; fp16 taken at the same rate"
                                % (peak_key, peak_src),
                 "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak))}
-    roof["traffic_note"] = "see profiles/ for ncu DRAM bytes" if unfused else ("DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum); "
+    roof["traffic_note"] = ("DRAM bytes per step, summed over its three kernels (ncu "
+                            "dram__bytes_read.sum + dram__bytes_write.sum)") if unfused else ("DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum); "
                             "algorithmic compulsory bytes (Q+K+V read, O+LSE write): %d" % w_bytes(w))
     if unfused or rowwise:
         line_extra = {"impl": args.impl}
