@@ -66,7 +66,8 @@ BWD_FLOP_FACTOR = 2.5
 # was taken.  Reported only while those sources still hash the same; null
 # once the kernel has changed.
 KERNEL_SOURCES = {"tc": ["fwd_tc.cu", "sm103_ptx.cuh"], "ffma": ["fwd_ffma.cu"],
-                  "unfused": ["fwd_unfused.cu", "sm103_ptx.cuh"]}
+                  "unfused": ["fwd_unfused.cu", "sm103_ptx.cuh"],
+                  "bwd": ["bwd_tc.cu", "sm103_ptx.cuh"]}
 NCU_TRAFFIC = {
     "bf16_B4_H16_N4096_D128": (201401344 + 37754624, "0ad671d8eedf986a"),
     "bf16_B2_H32_N8192_D128_causal_qstd4": (2534908928 + 127398912, "0ad671d8eedf986a"),
@@ -80,6 +81,14 @@ NCU_TRAFFIC_UNFUSED = {
     "bf16_B4_H16_N4096_D128": (6654303488 + 6404445952, "eea14f381a5e072c"),
     "bf16_B2_H32_N8192_D128_causal_qstd4": (13389511424 + 13121869568, "eea14f381a5e072c"),
     "fp16_B1_H16_N16000_D64_causal": (12438579200 + 12321152000, "eea14f381a5e072c"),
+}
+
+
+# The backward: DRAM bytes of one step (statistics, dK/dV and dQ kernels).
+NCU_TRAFFIC_BWD = {
+    "bf16_B4_H16_N4096_D128": (676751616 + 154443008, "b62632c1e8d7d51e"),
+    "bf16_B2_H32_N8192_D128_causal_qstd4": (7975664384 + 355521280, "b62632c1e8d7d51e"),
+    "fp16_B1_H16_N16000_D64_causal": (463883776 + 50837760, "b62632c1e8d7d51e"),
 }
 
 
@@ -97,9 +106,11 @@ def kernel_source_hash(family):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(w, unfused=False):
-    entry = (NCU_TRAFFIC_UNFUSED if unfused else NCU_TRAFFIC).get(w.name)
-    if entry is None or entry[1] != kernel_source_hash("unfused" if unfused else kernel_family(w)):
+def ncu_traffic(w, unfused=False, bwd=False):
+    table = NCU_TRAFFIC_BWD if bwd else (NCU_TRAFFIC_UNFUSED if unfused else NCU_TRAFFIC)
+    family = "bwd" if bwd else ("unfused" if unfused else kernel_family(w))
+    entry = table.get(w.name)
+    if entry is None or entry[1] != kernel_source_hash(family):
         return None
     return entry[0]
 
@@ -540,7 +551,9 @@ def run_ours_bwd(args, w, ws, rank, local):
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
-            "traffic": None, "scope": "the whole three-kernel step (statistics, dK/dV, dQ)",
+            "traffic": ncu_traffic(w, bwd=True), "scope": "the whole three-kernel step (statistics, dK/dV, dQ)",
+            "traffic_note": "DRAM bytes per step, summed over its three kernels (ncu "
+                            "dram__bytes_read.sum + dram__bytes_write.sum)",
             "peak_source": "bf16_tflops dense bf16 (cuBLAS burst) of %s; fp16 taken at the same rate" % peak_src,
             "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
             "executed_tensor_tflops": achieved * 7.0 / 5.0,
