@@ -12,10 +12,10 @@
 //   prep : per row, Delta_i and LSE_i * log2(e) into a padded workspace
 //          (+inf / 0 past N so that tail rows contribute nothing);
 //   dKdV : one CTA per (head, 128-key block): K and V stay in shared memory
-//          while the 128-query tiles of Q, dO and their row statistics stream
-//          through a TMA ring; S^T = K Q^T and dP^T = V dO^T land in TMEM,
-//          eight warps (one key row per thread, two warps per row range,
-//          64 columns each) turn them into P^T and dS^T
+//          while 64-query tiles of Q, dO and their row statistics stream
+//          through a TMA ring; S^T = K Q^T and dP^T = V dO^T land in TMEM
+//          (two buffers), eight warps (one key row per thread, two warps per
+//          row range, 32 columns each) turn them into P^T and dS^T
 //          (16-bit, written back into TMEM), and dV += P^T dO, dK += dS^T Q
 //          accumulate in TMEM; dK and dV are written once at the end;
 //   dQ   : one CTA per (head, 128-query tile), the mirror image: Q and dO
