@@ -155,8 +155,9 @@ FATTN_API int fattn_fwd_host(const void* q_host, const void* k_host, const void*
 
 /*
  * fattn_bwd_workspace_bytes -- bytes of device workspace fattn_bwd needs:
- * fp32 [B*H][2][Npad] (per row LSE*log2(e) and Delta = dO.O, Npad = N
- * rounded up to 128), i.e. 8 * B*H*Npad.  0 for an empty or invalid size.
+ * fp32 [B*H][2][Npad] (per row -LSE*log2(e) and -Delta, Delta = dO.O,
+ * Npad = N rounded up to 128), i.e. 8 * B*H*Npad.  0 for an empty or
+ * invalid size.
  */
 FATTN_API int64_t fattn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N);
 

@@ -9,8 +9,9 @@
 // where Delta_i = dO_i . O_i.
 //
 // Three kernels:
-//   prep : per row, Delta_i and LSE_i * log2(e) into a padded workspace
-//          (+inf / 0 past N so that tail rows contribute nothing);
+//   prep : per row, -LSE_i * log2(e) and -Delta_i into a padded workspace
+//          (-inf / 0 past N so that tail rows contribute nothing), negated so
+//          that the elementwise steps are plain packed adds and FMAs;
 //   dKdV : one CTA per (head, 128-key block): K and V stay in shared memory
 //          while 64-query tiles of Q, dO and their row statistics stream
 //          through a TMA ring; S^T = K Q^T and dP^T = V dO^T land in TMEM
@@ -103,6 +104,31 @@ __device__ __forceinline__ BwdBars bwd_bars(uint8_t* smem) {
     b.abort_flag = reinterpret_cast<uint32_t*>(b.done + 1);
     b.tmem_slot = b.abort_flag + 1;
     return b;
+}
+
+// (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1), (a0 + b0, a1 + b1), (a0 * b0, a1 * b1):
+// one packed fp32 instruction each, rounded as the scalar forms.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 __device__ __forceinline__ uint32_t pack16(float lo, float hi, bool bf16) {
@@ -452,11 +478,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         const int row = blk0 + r;  // KV: key index; dQ: query index
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const int c0 = half * 64;  // first column of this warp
-        float lse2_r = 0.f, delta_r = 0.f;
+        float nlse2_r = 0.f, ndelta_r = 0.f;  // -LSE*log2(e) and -Delta of this row
         if (!KV) {
             const float* stats = a.ws + static_cast<int64_t>(tk.bh) * 2 * a.Npad + row;
-            lse2_r = stats[0];        // +inf past N: the row's P is 0
-            delta_r = stats[a.Npad];
+            nlse2_r = stats[0];        // -inf past N: the row's P is 0
+            ndelta_r = stats[a.Npad];
         }
         bool ok = true;
         if (KV) {
@@ -471,9 +497,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                     ok = warp_wait(&bars.full_a[sa], (it / L::kSA) & 1u, bars.abort_flag, a.timeout_ns);
                 if (!ok) break;
                 tc_fence_after();
-                const float* lse2s = reinterpret_cast<const float*>(smem + L::kRingA + sa * L::kSlotA +
-                                                                    2 * L::kTileIn);
-                const float* deltas = lse2s + kBQ;
+                const float* nlse2s = reinterpret_cast<const float*>(smem + L::kRingA + sa * L::kSlotA +
+                                                                     2 * L::kTileIn);
+                const float* ndeltas = nlse2s + kBQ;
                 // queries before this key row exist only in the tiles that meet the block's diagonal
                 const bool diag = CAUSAL && jq < 2 * tk.blk + 2;
                 const int qoff = jq * kBQ - blk0;  // query - key = qoff + col - r
@@ -484,20 +510,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                 tmem_wait_ld();
                 reg_fence(sv);
                 reg_fence(dpv);
+                // P^T = exp2(s*scale*log2e - LSE2) and dS^T = P^T (dP^T - Delta),
+                // two queries per packed instruction; the statistics of the
+                // warp's 32 queries come as 16-byte broadcasts.
                 uint32_t pk[16], dsk[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float p[2], ds[2];
+                for (int e4 = 0; e4 < 32; e4 += 4) {
+                    const float4 nl = *reinterpret_cast<const float4*>(nlse2s + 32 * half + e4);
+                    const float4 nd = *reinterpret_cast<const float4*>(ndeltas + 32 * half + e4);
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int col = 32 * half + e + u;  // query jq*64 + col
-                        float pv = ex2_approx(__uint_as_float(sv[e + u]) * a.sl2 - lse2s[col]);
-                        if (diag && qoff + col < r) pv = 0.f;
-                        p[u] = pv;
-                        ds[u] = pv * (__uint_as_float(dpv[e + u]) - deltas[col]);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int e = e4 + 2 * h2;
+                        const float nl0 = h2 ? nl.z : nl.x, nl1 = h2 ? nl.w : nl.y;
+                        const float nd0 = h2 ? nd.z : nd.x, nd1 = h2 ? nd.w : nd.y;
+                        float x0, x1, d0, d1;
+                        fma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), a.sl2, a.sl2,
+                             nl0, nl1);
+                        float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        if (diag) {  // queries before this key row are masked
+                            const int col = 32 * half + e;  // query jq*64 + col
+                            if (qoff + col < r) p0 = 0.f;
+                            if (qoff + col + 1 < r) p1 = 0.f;
+                        }
+                        add2(d0, d1, __uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1]), nd0, nd1);
+                        mul2(d0, d1, p0, p1, d0, d1);
+                        pk[e / 2] = pack16(p0, p1, BF16);
+                        dsk[e / 2] = pack16(d0, d1, BF16);
                     }
-                    pk[e / 2] = pack16(p[0], p[1], BF16);
-                    dsk[e / 2] = pack16(ds[0], ds[1], BF16);
                 }
                 tmem_st16(sb, pk);
                 tmem_st16(sb + 16, dsk);
@@ -533,19 +572,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                     tmem_wait_ld();
                     reg_fence(sv);
                 }
+                // dS = exp2(s*scale*log2e - LSE2) (dP - Delta), two keys per
+                // packed instruction; keys past N or (diagonal tile) past the
+                // row are masked only in chunks that hold such keys.
+                const int vis = min(a.N - j * kBT, diag ? r + 1 : kBT) - (c0 + c * 32);
+                const bool masked = __any_sync(0xffffffffu, vis < 32);
                 uint32_t dsk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    float ds[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int col = c0 + c * 32 + e + u;  // key j*128+col
-                        float pv = ex2_approx(__uint_as_float(sv[e + u]) * a.sl2 - lse2_r);
-                        const int key = j * kBT + col;
-                        if (key >= a.N || (diag && col > r)) pv = 0.f;
-                        ds[u] = pv * (__uint_as_float(dpv[c][e + u]) - delta_r);
+                    float x0, x1, d0, d1;
+                    fma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), a.sl2, a.sl2,
+                         nlse2_r, nlse2_r);
+                    float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    if (masked) {
+                        if (e >= vis) p0 = 0.f;
+                        if (e + 1 >= vis) p1 = 0.f;
                     }
-                    dsk[e / 2] = pack16(ds[0], ds[1], BF16);
+                    add2(d0, d1, __uint_as_float(dpv[c][e]), __uint_as_float(dpv[c][e + 1]), ndelta_r,
+                         ndelta_r);
+                    mul2(d0, d1, p0, p1, d0, d1);
+                    dsk[e / 2] = pack16(d0, d1, BF16);
                 }
                 // Only columns of this chunk, already read, are overwritten.
                 tmem_st16(sb + c * 32, dsk);
@@ -594,9 +640,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
     }
 }
 
-// Delta_i = dO_i . O_i (fp32 over the 16-bit inputs) and LSE_i * log2(e),
-// one warp per row of the padded workspace [B*H][2][Npad]; rows past N get
-// +inf and 0.
+// -LSE_i * log2(e) and -Delta_i, Delta_i = dO_i . O_i (fp32 over the 16-bit
+// inputs), one warp per row of the padded workspace [B*H][2][Npad]; rows
+// past N get -inf and 0.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const void* __restrict__ o,
                                                             const void* __restrict__ dout,
@@ -608,7 +654,7 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const void* __restri
     if (gw >= rows_padded) return;
     const int64_t bh = gw / Npad;
     const int i = static_cast<int>(gw % Npad);
-    float lse2 = INFINITY, delta = 0.f;
+    float nlse2 = -INFINITY, ndelta = 0.f;
     if (i < N) {
         const int64_t row = bh * N + i;
         constexpr int kPer = D / 32;  // 16-bit elements per lane: 2 or 4
@@ -629,12 +675,12 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const void* __restri
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        delta = acc;
-        lse2 = lse[row] * 1.4426950408889634f;
+        ndelta = -acc;
+        nlse2 = -lse[row] * 1.4426950408889634f;
     }
     if (lane == 0) {
-        ws[bh * 2 * Npad + i] = lse2;
-        ws[(bh * 2 + 1) * Npad + i] = delta;
+        ws[bh * 2 * Npad + i] = nlse2;
+        ws[(bh * 2 + 1) * Npad + i] = ndelta;
     }
 }
 
