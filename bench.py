@@ -86,9 +86,9 @@ NCU_TRAFFIC_UNFUSED = {
 
 # The backward: DRAM bytes of one step (statistics, dK/dV and dQ kernels).
 NCU_TRAFFIC_BWD = {
-    "bf16_B4_H16_N4096_D128": (676751616 + 154443008, "1074d6b858040c98"),
-    "bf16_B2_H32_N8192_D128_causal_qstd4": (7975664384 + 355521280, "1074d6b858040c98"),
-    "fp16_B1_H16_N16000_D64_causal": (463883776 + 50837760, "1074d6b858040c98"),
+    "bf16_B4_H16_N4096_D128": (676511232 + 154823680, "83158358f7612600"),
+    "bf16_B2_H32_N8192_D128_causal_qstd4": (7986440960 + 355387648, "83158358f7612600"),
+    "fp16_B1_H16_N16000_D64_causal": (460794368 + 51374592, "83158358f7612600"),
 }
 
 
