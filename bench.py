@@ -36,6 +36,10 @@ roofline is the HBM bound of the whole three-kernel step.
 
 `--impl rowwise` (fp32 workloads) times fattn_fwd_f32_rowwise, the fp32
 kernel with one query row per thread, under the same rules (no e2e leg).
+
+`--hkv G` times the grouped-query form of a 16-bit workload (forward or
+backward): K and V are the workload's first G heads, shared by H/G query
+heads each; FLOP as for the multi-head workload; device buffers only.
 """
 import argparse
 import json
@@ -180,8 +184,8 @@ def unfused_bytes(w):
     return w_bytes(w) + bh * (2 * 4 * s_elems + 2 * e * p_elems)
 
 
-def config_of(w, n_gpus):
-    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "dtype": w.dtype,
+def config_of(w, n_gpus, hkv=0):
+    return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": hkv or w.H, "N": w.N, "D": w.D, "dtype": w.dtype,
             "causal": w.causal, "q_std": w.q_std, "scale": w.scale, "seed": w.seed,
             "l2": "flushed before every timed step (512 MB rewrite outside the events)",
             "parallelism": "replicas x%d (no exchange step)" % n_gpus}
@@ -292,6 +296,8 @@ def run_ours(args, w, ws, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     q, k, v = workload_inputs(w)
+    if args.hkv:  # grouped-query heads: the first Hkv heads of the workload's K and V
+        k, v = k[:, :args.hkv].contiguous(), v[:, :args.hkv].contiguous()
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     o = torch.empty_like(qd)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
@@ -383,12 +389,12 @@ def run_ours(args, w, ws, rank, local):
         sm_mhz = peaks.get("sm_max_mhz", 2070.0)
         peak = torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT,
-                "frac": achieved / peak, "traffic": ncu_traffic(w) if not rowwise else None,
+                "frac": achieved / peak, "traffic": ncu_traffic(w) if not (rowwise or args.hkv) else None,
                 "peak_source": "FP32 FFMA: SMs x 128 lanes x 2 FLOP x max SM clock (%s clock)" % peak_src}
     else:
         peak = float(peaks[peak_key])
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                "frac": achieved / peak, "traffic": ncu_traffic(w) if not rowwise else None,
+                "frac": achieved / peak, "traffic": ncu_traffic(w) if not (rowwise or args.hkv) else None,
                 "peak_source": "%s dense bf16 (cuBLAS burst) of %s; fp16 taken at the same rate"
                                % (peak_key, peak_src),
                 "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak))}
@@ -404,7 +410,7 @@ def run_ours(args, w, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_median": statistics.median(per),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": DTYPE_NAMES[w.dtype], "data": "synthetic (seeded iid normal Q, K, V)",
-        "config": config_of(w, ws), "pct_of_peak": 100.0 * roof["frac"], "roofline": roof,
+        "config": config_of(w, ws, args.hkv), "pct_of_peak": 100.0 * roof["frac"], "roofline": roof,
         "e2e": ({"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                  "ms_per_step": e2e_ms, "api": "fattn_fwd_host (pinned host buffers)"}
@@ -467,9 +473,11 @@ def run_ours_bwd(args, w, ws, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     q, k, v, do = bwd_inputs(w)
+    if args.hkv:  # grouped-query heads: the first Hkv heads of the workload's K and V
+        k, v = k[:, :args.hkv].contiguous(), v[:, :args.hkv].contiguous()
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     o, lse = fattn.fwd(qd, kd, vd, causal=w.causal, scale=w.scale)
-    dq, dk, dv = (torch.empty_like(qd) for _ in range(3))
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
     wsp = torch.empty(fattn.bwd_workspace_bytes(w.B, w.H, w.N), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -551,7 +559,8 @@ def run_ours_bwd(args, w, ws, rank, local):
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
-            "traffic": ncu_traffic(w, bwd=True), "scope": "the whole three-kernel step (statistics, dK/dV, dQ)",
+            "traffic": ncu_traffic(w, bwd=True) if not args.hkv else None,
+            "scope": "the whole three-kernel step (statistics, dK/dV, dQ)",
             "traffic_note": "DRAM bytes per step, summed over its three kernels (ncu "
                             "dram__bytes_read.sum + dram__bytes_write.sum)",
             "peak_source": "bf16_tflops dense bf16 (cuBLAS burst) of %s; fp16 taken at the same rate" % peak_src,
@@ -564,7 +573,7 @@ def run_ours_bwd(args, w, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_median": statistics.median(per),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": DTYPE_NAMES[w.dtype], "data": "synthetic (seeded iid normal Q, K, V, dO)",
-        "config": dict(config_of(w, ws), **{"pass": "bwd"}), "pct_of_peak": 100.0 * roof["frac"],
+        "config": dict(config_of(w, ws, args.hkv), **{"pass": "bwd"}), "pct_of_peak": 100.0 * roof["frac"],
         "roofline": roof,
         "e2e": ({"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
@@ -670,6 +679,9 @@ def main():
     ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference", "unfused", "rowwise"])
     ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"])
+    ap.add_argument("--hkv", type=int, default=0,
+                    help="grouped-query K/V heads (0: as many as query heads); 16-bit workloads, "
+                         "device-buffer timing only")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall time of the CPU oracle sample (cpu_baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -679,6 +691,11 @@ def main():
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_env()
     w = BY_NAME[args.workload]
+    if args.hkv:
+        if args.impl != "ours" or w.dtype == "fp32" or w.H % args.hkv != 0 or args.hkv >= w.H:
+            ap.error("--hkv needs --impl ours, a 16-bit workload and 0 < Hkv < H dividing H")
+        args.no_e2e = True           # the host-buffer entry points take H == Hkv
+        args.no_cpu_baseline = True
     if args.pass_ == "bwd":
         if args.impl in ("unfused", "rowwise"):
             ap.error("--impl %s is a forward variant" % args.impl)
