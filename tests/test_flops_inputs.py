@@ -73,3 +73,36 @@ def test_unfused_algorithmic_bytes():
     # a causal S/P triangle costs a bit over half of the square
     full = 16000 * 16000
     assert 0.5 < elems / full < 0.51
+
+
+def test_recorded_traffic_follows_the_kernel_sources():
+    """bench.py reports a recorded ncu DRAM figure only while the kernel
+    sources it was captured on still hash the same, and null otherwise."""
+    import bench
+    from tiled_attention_forward_gb300.inputs import BY_NAME
+    w = BY_NAME["bf16_B4_H16_N4096_D128"]
+    for table, kw in ((bench.NCU_TRAFFIC, {}), (bench.NCU_TRAFFIC_BWD, {"bwd": True}),
+                      (bench.NCU_TRAFFIC_UNFUSED, {"unfused": True})):
+        value, tag = table[w.name]
+        assert bench.ncu_traffic(w, **kw) == (value if tag == bench.kernel_source_hash(
+            "bwd" if kw.get("bwd") else ("unfused" if kw.get("unfused") else "tc")) else None)
+        saved = table[w.name]
+        try:
+            table[w.name] = (value, "0" * 16)
+            assert bench.ncu_traffic(w, **kw) is None
+        finally:
+            table[w.name] = saved
+    # every recorded figure at least covers the DRAM bytes the workload must move
+    for name, (value, _) in bench.NCU_TRAFFIC.items():
+        assert value >= 0.8 * bench.w_bytes(BY_NAME[name])
+
+
+def test_bench_rejects_bad_hkv():
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for extra in (["--hkv", "3"], ["--hkv", "16"], ["--hkv", "4", "--impl", "unfused"],
+                  ["--hkv", "4", "--workload", "fp32_B4_H8_N8192_D64_causal"]):
+        r = subprocess.run([sys.executable, os.path.join(root, "bench.py")] + extra,
+                           capture_output=True, text=True, timeout=300)
+        assert r.returncode == 2 and "--hkv needs" in r.stderr
