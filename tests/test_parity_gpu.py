@@ -59,6 +59,15 @@ def test_tensor_core_large_scores(causal):
     run_case(1, 4, 700, 128, "bf16", causal, seed=400, q_std=4.0)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_tensor_core_large_scores_d64(dtype, causal):
+    """The same at D = 64, where the two Q tiles rotate through three S
+    buffers and an O rescale first waits for the tile's previous P.V product;
+    B*H*blocks well above the SM count so buffers and phases wrap many times."""
+    run_case(2, 24, 700, 64, dtype, causal, seed=410, q_std=4.0)
+
+
 def test_ffma_many_blocks():
     run_case(2, 3, 1100, 64, "fp32", True, seed=500)
 
