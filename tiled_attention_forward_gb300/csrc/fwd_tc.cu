@@ -254,12 +254,14 @@ __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (one warp; one elected lane issues MMAs and commits)
+// MMA issuer, two-buffer layout (D = 128; one warp, one elected lane issues
+// MMAs and commits)
 // ---------------------------------------------------------------------------
 template <int D, bool BF16, bool CAUSAL>
 __device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint32_t tmem_base,
                          volatile uint32_t* abort_flag) {
     using L = TcLayout<D>;
+    static_assert(!L::kRot, "the three-buffer layout has its own MMA role");
     constexpr uint32_t kIdescQK = idesc_f16_f32(kTcBM, kTcBN, BF16 ? 1u : 0u, 0u, 0u);
     constexpr uint32_t kIdescPV = idesc_f16_f32(kTcBM, D, BF16 ? 1u : 0u, 0u, 1u);
     const uint32_t q_smem = smem_u32(smem + L::kQOff);
@@ -339,42 +341,28 @@ __device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint3
         for (int j = 0; j < tk.nbmax && ok; ++j) {
             const bool has_next = j + 1 < tk.nbmax;
             // Any barrier test issued right after an MMA group waits for that
-            // group to be taken by the tensor pipe, so the tests are batched
-            // where that costs nothing else.  With a deep K/V ring (D = 64:
-            // eight stages) K_{j+1} has long landed when P_0 is ready, and V_j,
-            // K_{j+1}, P_0 are tested together before tile 0's MMAs.  With the
-            // five-stage ring of D = 128 a K tile is often still in flight
-            // then, so P.V_0 is issued first and K_{j+1} waited for after it.
-            constexpr bool kEarlyK = L::kStages >= 8;
+            // group to be taken by the tensor pipe.  With the five-stage ring
+            // a K tile is often still in flight when P_0 is ready, so P.V_0 is
+            // issued first and K_{j+1} waited for after it.
             wait_slot(vslot);  // V_j
             if (!ok) break;
-            if (kEarlyK && has_next) {
-                wait_slot(kslot);  // K_{j+1}
-                if (!ok) break;
-            }
             for (int i = 0; i < 2 && ok; ++i) {
                 if (j < tk.nb[i]) {
                     ok = warp_wait(&bars.p_full[i], pcnt[i] & 1u, abort_flag, a.timeout_ns);
                     ++pcnt[i];
                     if (!ok) break;
                     tc_fence_after();
-                    if (!kEarlyK) {
-                        if (elect_one_sync()) {
-                            issue_pv(i, vslot, j > 0);
-                            if (j == tk.nb[i] - 1) mma_commit(&bars.o_full[i]);
-                        }
-                        __syncwarp();
+                    if (elect_one_sync()) {
+                        issue_pv(i, vslot, j > 0);
+                        if (j == tk.nb[i] - 1) mma_commit(&bars.o_full[i]);
                     }
+                    __syncwarp();
                 }
-                if (!kEarlyK && i == 0 && has_next) {
+                if (i == 0 && has_next) {
                     wait_slot(kslot);  // K_{j+1}
                     if (!ok) break;
                 }
                 if (elect_one_sync()) {
-                    if (kEarlyK && j < tk.nb[i]) {
-                        issue_pv(i, vslot, j > 0);
-                        if (j == tk.nb[i] - 1) mma_commit(&bars.o_full[i]);
-                    }
                     if (j + 1 < tk.nb[i]) {
                         issue_qk(i, kslot);
                         mma_commit(&bars.s_full[i]);
