@@ -68,7 +68,7 @@ typedef enum {
 typedef enum {
     FATTN_OK = 0,
     FATTN_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad dtype, non-finite or negative scale, overlapping O */
-    FATTN_ERR_UNSUPPORTED = 2,   /* D not in {64, 128}; N*D, B*H or N beyond the kernels' index range */
+    FATTN_ERR_UNSUPPORTED = 2,   /* D not in {64, 128}; N or B*H above 2^30, or B*H*N*D above 2^52 */
     FATTN_ERR_MISALIGNED = 3,    /* a tensor pointer not 16-byte aligned (TMA / vector access requirement) */
     FATTN_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (launch, copy, tensor-map encode) */
     FATTN_ERR_TIMEOUT = 5,       /* a kernel's bounded wait expired (reported by fattn_get_device_status) */

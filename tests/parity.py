@@ -5,47 +5,84 @@ method's target states:
   * fp32:        max |O - O_ref| <= 1e-4;
   * LSE (fp32, natural log): max |LSE - LSE_ref| <= 1e-3.
 
-One documented allowance: the result O is delivered in the input dtype, and
-rounding the exact result to bf16 alone moves it by up to half a bf16 ulp,
-which is 2^-7 ~ 0.0078 for |O| in [2, 4) and 2^-6 ~ 0.0156 for |O| in [4, 8):
-more than the 1e-2 gate by itself.  Where that half ulp exceeds 2^-8 (bf16
-|O| >= 2; fp16 |O| >= 16) the per-element bound is 1e-2 plus the half ulp of
-the output dtype at the reference value; everywhere else it is exactly 1e-2.
+O is delivered in the input dtype.  Rounding the exact result to bf16 alone
+moves it by up to half a bf16 ulp, 2^-7 ~ 0.0078 for |O| in [2, 4) and
+2^-6 ~ 0.0156 for |O| in [4, 8), so an element can miss the flat 1e-2 gate
+with no error at all before the output rounding.  Such an element is
+accepted only where the output rounding explains it:
+
+  * half an ulp of the output dtype at the oracle's value exceeds 2^-8
+    (bf16 |O| >= 2, fp16 |O| >= 16; below that the flat gate applies
+    unchanged);
+  * some value within 1e-2 of the oracle rounds to the delivered value: the
+    delivered value's rounding interval (half its ulp on each side) meets
+    [O_ref - 1e-2, O_ref + 1e-2];
+  * the delivered value is the oracle's own rounding to the output dtype or
+    one of its two neighbours.
+
+The number of such elements is counted in the statistics (``n_over_gate``)
+and reported.  Asking instead that they lie within 1e-2 of the oracle rounded
+to the output dtype cannot work for bf16 |O| in [2, 4): an element more than
+1e-2 (> half an ulp) from the oracle never shares its rounding, so its
+distance to the rounded oracle is a whole ulp, 2^-6 > 1e-2, whatever the
+error before rounding.
 """
 import numpy as np
 import torch
 
 MANTISSA_BITS = {torch.bfloat16: 7, torch.float16: 10, torch.float32: 23}
+MIN_NORMAL_EXP = {torch.bfloat16: -126, torch.float16: -14, torch.float32: -126}
+GATE = {torch.bfloat16: 1e-2, torch.float16: 1e-2, torch.float32: 1e-4}
+
+# Statistics of the comparisons a test asks to have reported at the end of the
+# run (tests/conftest.py prints them).
+REPORTED = []
+
+
+def ulp(x, dtype):
+    """Spacing of `dtype` numbers at |x| (subnormals: the smallest normal spacing)."""
+    a = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** MIN_NORMAL_EXP[dtype])))
+    return np.exp2(e - MANTISSA_BITS[dtype])
 
 
 def half_ulp(ref, dtype):
-    """Half a unit in the last place of `dtype` at |ref| (normal range)."""
-    a = np.abs(np.asarray(ref, np.float64))
-    e = np.floor(np.log2(np.maximum(a, 2.0 ** -60)))
-    return np.exp2(e - MANTISSA_BITS[dtype] - 1)
+    """Half a unit in the last place of `dtype` at |ref|."""
+    return 0.5 * ulp(ref, dtype)
 
 
-def o_bounds(ref, dtype):
-    if dtype == torch.float32:
-        return np.full(np.shape(ref), 1e-4)
-    hu = half_ulp(ref, dtype)
-    return np.where(hu > 2.0 ** -8, 1e-2 + hu, 1e-2)
+def round_to(x, dtype):
+    """x (fp64) rounded to `dtype` and widened back to fp64."""
+    return torch.from_numpy(np.ascontiguousarray(x, np.float64)).to(dtype).to(torch.float64).numpy()
 
 
-def compare(o_gpu, o_ref, lse_gpu, lse_ref, dtype, what=""):
+def compare(o_gpu, o_ref, lse_gpu, lse_ref, dtype, what="", report=False):
     """Raise AssertionError with statistics if the GPU result misses the gate."""
     o_gpu = np.asarray(o_gpu, np.float64)
     o_ref = np.asarray(o_ref, np.float64)
     assert o_gpu.shape == o_ref.shape, (o_gpu.shape, o_ref.shape)
     assert np.all(np.isfinite(o_gpu)), "%s: non-finite output" % what
+    gate = GATE[dtype]
     err = np.abs(o_gpu - o_ref)
-    bound = o_bounds(o_ref, dtype)
-    stats = dict(max_abs=float(err.max()) if err.size else 0.0,
+    over = err > gate
+    stats = dict(n=int(err.size),
+                 max_abs=float(err.max()) if err.size else 0.0,
                  mean_abs=float(err.mean()) if err.size else 0.0,
-                 over_1e2=int((err > 1e-2).sum()),
+                 n_over_gate=int(over.sum()),
                  worst_ref=float(np.abs(o_ref).ravel()[int(err.argmax())]) if err.size else 0.0)
-    bad = err > bound
-    assert not bad.any(), "%s: %d elements over the bound %s" % (what, int(bad.sum()), stats)
+    if over.any():
+        g, r = o_gpu[over], o_ref[over]
+        # (0) only where output rounding alone can come near the gate
+        unexplained = half_ulp(r, dtype) <= 2.0 ** -8
+        # (1) a value within the gate of the oracle rounds to the delivered one
+        unexplained |= np.abs(g - r) > gate + half_ulp(g, dtype)
+        # (2) the delivered value is the oracle's rounding or a neighbour of it
+        off_by = np.abs(g - round_to(r, dtype)) / ulp(g, dtype)
+        unexplained |= off_by > 1.0 + 1e-9
+        stats["over_gate_max_abs"] = float(np.abs(g - r).max())
+        stats["over_gate_max_ulps_from_rounded_oracle"] = float(off_by.max())
+        assert not unexplained.any(), "%s: %d elements over the gate not explained by output rounding %s" % (
+            what, int(unexplained.sum()), stats)
     if dtype != torch.float32:
         assert stats["mean_abs"] <= 1e-3, "%s: mean abs %s" % (what, stats)
     if lse_gpu is not None:
@@ -55,6 +92,8 @@ def compare(o_gpu, o_ref, lse_gpu, lse_ref, dtype, what=""):
         lerr = float(np.abs(lse_gpu - lse_ref).max()) if lse_gpu.size else 0.0
         stats["lse_max_abs"] = lerr
         assert lerr <= 1e-3, "%s: LSE max abs %.3e" % (what, lerr)
+    if report:
+        REPORTED.append((what, stats))
     return stats
 
 
@@ -63,8 +102,8 @@ def to_f64(t):
 
 
 def sample_rows(B, H, N, count, seed, causal):
-    """Rows checked on a full-size workload: every row of the first and last
-    head's first and last 64 rows, plus `count` random (head, row) pairs."""
+    """Rows checked on a large problem: every row of the first and last head's
+    first and last 64 rows, plus `count` random (head, row) pairs."""
     r = np.random.default_rng(seed)
     bh = [0] * min(N, 64) + [B * H - 1] * min(N, 64)
     rows = list(range(min(N, 64))) + list(range(max(0, N - 64), N))
@@ -73,6 +112,24 @@ def sample_rows(B, H, N, count, seed, causal):
     bh += list(r.integers(0, B * H, count))
     rows += list(r.integers(0, N, count))
     return np.asarray(bh, np.int64), np.asarray(rows, np.int64)
+
+
+def workload_rows(B, H, N, per_head, seed):
+    """Rows checked on a full-size workload: every row of the first and of the
+    last head, plus `per_head` random rows of every head (drawn without
+    replacement within the head)."""
+    r = np.random.default_rng(seed)
+    BH = B * H
+    heads = [0] if BH == 1 else [0, BH - 1]
+    bh = [np.full(N, h, np.int64) for h in heads]
+    rows = [np.arange(N, dtype=np.int64) for _ in heads]
+    k = min(per_head, N)
+    for h in range(BH):
+        if h in heads:
+            continue
+        bh.append(np.full(k, h, np.int64))
+        rows.append(np.sort(r.choice(N, size=k, replace=False)).astype(np.int64))
+    return np.concatenate(bh), np.concatenate(rows)
 
 
 # ---------------------------------------------------------------------------

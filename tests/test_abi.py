@@ -82,6 +82,10 @@ def test_argument_errors_before_any_cuda_call(lib):
     assert call_fwd(lib, N=(1 << 30) + 1) == UNSUPPORTED
     assert call_fwd(lib, B=1 << 16, H=1 << 16) == UNSUPPORTED
     assert call_fwd(lib, B=70000, H=1, dtype=0) == UNSUPPORTED
+    # B*H*N*D past 2^52 elements (each of N and B*H within its own limit): the
+    # byte counts of the overlap checks would overflow int64 otherwise
+    assert call_fwd(lib, B=1 << 15, H=1 << 15, N=1 << 30, D=128) == UNSUPPORTED
+    assert call_fwd(lib, B=1, H=1 << 20, N=1 << 30, D=64) == UNSUPPORTED
 
 
 def test_rowwise_argument_errors(lib):

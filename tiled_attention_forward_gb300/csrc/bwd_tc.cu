@@ -684,19 +684,6 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const void* __restri
     }
 }
 
-template <typename K>
-cudaError_t opt_in_smem(K* fn, int bytes, bool (&done)[kMaxDevices]) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices || !done[dev]) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
-    }
-    return cudaSuccess;
-}
-
 template <int D, bool BF16, bool CAUSAL>
 cudaError_t bwd_launch_all(const BwdArgs& a, const void* o, const void* dout, const float* lse,
                            cudaStream_t stream) {
@@ -707,14 +694,14 @@ cudaError_t bwd_launch_all(const BwdArgs& a, const void* o, const void* dout, co
     if (e != cudaSuccess) return e;
     const unsigned grid_kv = static_cast<unsigned>(static_cast<int64_t>(a.num_tiles) * a.BHkv);
     const unsigned grid_q = static_cast<unsigned>(static_cast<int64_t>(a.num_tiles) * a.BH);
-    static bool kv_done[kMaxDevices] = {};
-    static bool q_done[kMaxDevices] = {};
+    static std::atomic<bool> kv_done[kMaxDevices] = {};
+    static std::atomic<bool> q_done[kMaxDevices] = {};
     auto* kkv = attn_bwd_kernel<D, BF16, true, CAUSAL>;
-    if ((e = opt_in_smem(kkv, BwdLayout<D, true>::kBytes, kv_done)) != cudaSuccess) return e;
+    if ((e = opt_in_smem_once(kkv, BwdLayout<D, true>::kBytes, kv_done)) != cudaSuccess) return e;
     kkv<<<grid_kv, kBwdThreads, BwdLayout<D, true>::kBytes, stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     auto* kq = attn_bwd_kernel<D, BF16, false, CAUSAL>;
-    if ((e = opt_in_smem(kq, BwdLayout<D, false>::kBytes, q_done)) != cudaSuccess) return e;
+    if ((e = opt_in_smem_once(kq, BwdLayout<D, false>::kBytes, q_done)) != cudaSuccess) return e;
     kq<<<grid_q, kBwdThreads, BwdLayout<D, false>::kBytes, stream>>>(a);
     return cudaGetLastError();
 }

@@ -14,6 +14,12 @@ namespace fattn {
 namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per barrier wait
+constexpr int64_t kMaxElements = int64_t(1) << 52;      // bound of B*H*N*D accepted by validate()
+
+// The fixed array behind fattn_fwd_unfused_static and the size the header
+// promises are one number.
+static_assert(static_cast<long long>(kUnfusedStaticBytes) == FATTN_UNFUSED_STATIC_BYTES,
+              "static workspace size must match the public header");
 constexpr float kLog2e = 1.4426950408889634f;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u; }
@@ -41,11 +47,14 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
         return FATTN_OK;
     }
     // Index ranges: N and B*H fit int32 (kernel indices, TMA coordinates,
-    // grid.y <= 65535 on the FFMA path) and B*H*N*D stays well inside int64.
+    // grid.y <= 65535 on the FFMA path), and B*H*N*D is bounded by 2^52
+    // elements, so that every byte count formed below stays far inside int64
+    // (no device holds a problem anywhere near that size).
     if (N > (int64_t(1) << 30) || B > (int64_t(1) << 30) || H > (int64_t(1) << 30))
         return FATTN_ERR_UNSUPPORTED;
     const int64_t BH = B * H;
     if (BH > (int64_t(1) << 30)) return FATTN_ERR_UNSUPPORTED;
+    if (BH * N > kMaxElements / D) return FATTN_ERR_UNSUPPORTED;  // BH*N <= 2^60: no overflow
     if (dtype == FATTN_F32 && BH > 65535) return FATTN_ERR_UNSUPPORTED;
     if (!q || !k || !v || !o) return FATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FATTN_ERR_MISALIGNED;
@@ -86,17 +95,17 @@ int64_t kv_tiles_for(int64_t r0, int64_t rows, int64_t N, int64_t bc, bool causa
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    // Looked up once; a function-local static is initialised exactly once even
+    // when several host threads make their first call at the same time.
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult qres;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                              &qres) == cudaSuccess &&
             qres == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
     return fn;
 }
 

@@ -248,15 +248,9 @@ cudaError_t launch_ffma_row(const float* q, const float* k, const float* v, floa
                         int BH, int H, int Hkv, int N, float scale_log2, cudaStream_t stream) {
     using L = RowLayout<D, BC>;
     auto* fn = attn_fwd_ffma_row_kernel<D, BC, CAUSAL>;
-    static bool done[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<bool> done[kMaxDevices] = {};
+    cudaError_t e = opt_in_smem_once(fn, L::kBytes, done);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices || !done[dev]) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
-    }
     const int num_qblk = (N + L::kBr - 1) / L::kBr;
     dim3 grid(num_qblk, BH);
     fn<<<grid, L::kBr, L::kBytes, stream>>>(q, k, v, o, lse, N, num_qblk, H, Hkv, scale_log2);
@@ -494,15 +488,9 @@ cudaError_t launch_ffma_tiled(const float* q, const float* k, const float* v, fl
                               int BH, int H, int Hkv, int N, float scale_log2, cudaStream_t stream) {
     using L = TiledLayout<D, BC>;
     auto* fn = attn_fwd_ffma_tiled_kernel<D, BC, CAUSAL, MIN_BLOCKS>;
-    static bool done[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<bool> done[kMaxDevices] = {};
+    cudaError_t e = opt_in_smem_once(fn, L::kBytes, done);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices || !done[dev]) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
-    }
     const int num_qblk = (N + L::kBr - 1) / L::kBr;
     dim3 grid(num_qblk, BH);
     fn<<<grid, kTiledThreads, L::kBytes, stream>>>(q, k, v, o, lse, N, num_qblk, H, Hkv, scale_log2);

@@ -831,15 +831,9 @@ cudaError_t launch_one(const TcArgs& a, int grid, cudaStream_t stream) {
     auto* fn = attn_fwd_tc_kernel<D, BF16, CAUSAL>;
     // The opt-in above 48 KB of dynamic shared memory is per device: set it
     // once for every device this instantiation is launched on.
-    static bool done[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<bool> done[kMaxDevices] = {};
+    cudaError_t e = opt_in_smem_once(fn, L::kAlloc, done);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices || !done[dev]) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
-    }
     fn<<<grid, kTcThreads, L::kAlloc, stream>>>(a);
     return cudaGetLastError();
 }

@@ -389,28 +389,13 @@ __global__ void __launch_bounds__(128, 1) unfused_pv_kernel(const __grid_constan
     }
 }
 
-// Raises the dynamic shared-memory limit of one kernel once per device; each
-// call site passes its own flag array (the kernels share one signature).
-template <typename K>
-cudaError_t opt_in(K* fn, int bytes, bool (&done)[kMaxDevices]) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices || !done[dev]) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
-    }
-    return cudaSuccess;
-}
-
 template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_all(const UnfusedArgs& a, cudaStream_t stream) {
     const int nt = (a.N + kUT - 1) / kUT;
     auto* k1 = unfused_scores_kernel<D, BF16, CAUSAL>;
-    static bool k1_done[kMaxDevices] = {};
-    static bool k3_done[kMaxDevices] = {};
-    cudaError_t e = opt_in(k1, ScoreSmem::kBytes, k1_done);
+    static std::atomic<bool> k1_done[kMaxDevices] = {};
+    static std::atomic<bool> k3_done[kMaxDevices] = {};
+    cudaError_t e = opt_in_smem_once(k1, ScoreSmem::kBytes, k1_done);
     if (e != cudaSuccess) return e;
     k1<<<dim3(nt, nt, a.BH), 128, ScoreSmem::kBytes, stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -425,7 +410,7 @@ cudaError_t launch_all(const UnfusedArgs& a, cudaStream_t stream) {
     else unfused_softmax_long_kernel<BF16, CAUSAL><<<grid2, kSmThreads, 0, stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     auto* k3 = unfused_pv_kernel<D, BF16, CAUSAL>;
-    e = opt_in(k3, PvSmem<D>::kBytes, k3_done);
+    e = opt_in_smem_once(k3, PvSmem<D>::kBytes, k3_done);
     if (e != cudaSuccess) return e;
     k3<<<dim3(nt, a.BH), 128, PvSmem<D>::kBytes, stream>>>(a);
     return cudaGetLastError();

@@ -2,6 +2,7 @@
 // Not part of the public ABI (see include/fattn.h).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -9,6 +10,23 @@
 namespace fattn {
 
 constexpr int kMaxDevices = 64;
+
+// Raises one kernel's dynamic shared-memory limit once per device.  Each call
+// site passes its own flag array; the flags are atomics, so host threads that
+// launch at the same time never race on them (setting the attribute twice is
+// harmless).
+template <typename K>
+inline cudaError_t opt_in_smem_once(K* fn, int bytes, std::atomic<bool> (&done)[kMaxDevices]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool known = dev >= 0 && dev < kMaxDevices;
+    if (known && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    if (known) done[dev].store(true, std::memory_order_release);
+    return cudaSuccess;
+}
 
 // ---- tensor-core path (bf16 / fp16), fwd_tc.cu ------------------------------
 constexpr int kTcBM = 128;        // Q rows per MMA tile (tcgen05 M)

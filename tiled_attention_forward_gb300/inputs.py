@@ -55,7 +55,8 @@ WORKLOADS = [
     Workload("fp32_B1_H1_N256_D64", 1, 1, 256, 64, "fp32", False, 1000,
              note="small fp32 case, non-causal"),
     Workload("fp32_B4_H8_N8192_D64_causal", 4, 8, 8192, 64, "fp32", True, 1001,
-             note="CUDA-core FFMA path (fattn_fwd_f32_rowwise: one row per thread, Br=128, Bc=32)"),
+             note="CUDA-core FFMA path: fattn_fwd runs the register-tiled kernel (8-row micro-tiles, "
+                  "64-key K/V tiles); fattn_fwd_f32_rowwise keeps one row per thread, Br=128, Bc=32"),
     Workload("bf16_B4_H16_N4096_D128", 4, 16, 4096, 128, "bf16", False, 1002,
              note="tensor-core path, non-causal (headline)"),
     Workload("bf16_B2_H32_N8192_D128_causal_qstd4", 2, 32, 8192, 128, "bf16", True, 1003,
