@@ -21,7 +21,9 @@
 //              O_i += P_i V_j (TS form), tcgen05.commit -> mbarriers
 //   warp 9     TMA producer (one elected lane): Q tiles once per task, K/V tiles
 //              through a ring of shared-memory stages
-//   warps 10-11 idle
+//   warp 10    D = 128: the MMA warp's helper, which does the MMA warp's
+//              barrier waits and releases it on a named barrier
+//   warp 11    idle
 // The control warpgroup (warps 8-11) gives up registers (setmaxnreg) so the
 // softmax warpgroups can hold a whole 128-score row per thread: 168 per
 // thread at launch; 2 x 128 x kSoftmaxRegs + 128 x kControlRegs <= 384 x 168.
@@ -254,12 +256,22 @@ __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer, two-buffer layout (D = 128; one warp, one elected lane issues
-// MMAs and commits)
+// MMA issue, two-buffer layout (D = 128): an issuing warp and its helper warp
 // ---------------------------------------------------------------------------
-template <int D, bool BF16, bool CAUSAL>
-__device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint32_t tmem_base,
-                         volatile uint32_t* abort_flag) {
+// A barrier test (a shared-memory access) made by the warp that has just
+// issued MMAs waits until those MMAs are taken by the tensor pipe, so every
+// wait between two MMA groups left the pipe idle for the wake-up.  Here the
+// issuing warp never touches a barrier inside its loop: a helper warp runs
+// the same schedule, does every mbarrier wait, and meets the issuing warp on
+// a named barrier (kMmaSync) before each group that depends on a wait.  The
+// named barrier reduces the helper's "every wait succeeded" flag, so both
+// warps leave the schedule at the same point when a wait gives up.
+constexpr uint32_t kMmaSync = 1;          // named barrier id (0 is __syncthreads)
+constexpr uint32_t kMmaSyncThreads = 64;  // the issuing warp and its helper
+
+template <int D, bool BF16, bool CAUSAL, bool HELPER>
+__device__ void mma_pair_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint32_t tmem_base,
+                              volatile uint32_t* abort_flag) {
     using L = TcLayout<D>;
     static_assert(!L::kRot, "the three-buffer layout has its own MMA role");
     constexpr uint32_t kIdescQK = idesc_f16_f32(kTcBM, kTcBN, BF16 ? 1u : 0u, 0u, 0u);
@@ -267,17 +279,32 @@ __device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint3
     const uint32_t q_smem = smem_u32(smem + L::kQOff);
     const uint32_t kv_smem = smem_u32(smem + L::kKVOff);
 
-    uint32_t kv_it = 0;
+    uint32_t kv_it = 0;               // ring positions consumed (both warps count alike)
     uint32_t qcnt[2] = {0u, 0u};
     uint32_t pcnt[2] = {0u, 0u};
     bool ok = true;
 
-    auto wait_slot = [&](uint32_t& slot) {
+    // The helper's waits; the issuing warp only advances the same counters.
+    auto wait_kv = [&](uint32_t& slot) {
         slot = kv_it % L::kStages;
-        ok = warp_wait(&bars.kv_full[slot], (kv_it / L::kStages) & 1u, abort_flag, a.timeout_ns);
+        if (HELPER && ok)
+            ok = warp_wait(&bars.kv_full[slot], (kv_it / L::kStages) & 1u, abort_flag, a.timeout_ns);
         ++kv_it;
-        tc_fence_after();
     };
+    auto wait_q = [&](int i) {
+        if (HELPER && ok) ok = warp_wait(&bars.q_full[i], qcnt[i] & 1u, abort_flag, a.timeout_ns);
+    };
+    auto wait_p = [&](int i) {
+        if (HELPER && ok) ok = warp_wait(&bars.p_full[i], pcnt[i] & 1u, abort_flag, a.timeout_ns);
+        ++pcnt[i];
+    };
+    // Both warps pass here together; false when a wait of the helper gave up.
+    auto sync = [&]() -> bool {
+        ok = named_barrier_and(kMmaSync, kMmaSyncThreads, ok);
+        if (!HELPER) tc_fence_after();
+        return ok;
+    };
+
     // Descriptor templates with a zero start address.  A tile's descriptor is
     // the template plus (shared address >> 4): the start-address field is the
     // low 14 bits and every shared address is below 256 KB, so the add never
@@ -311,81 +338,92 @@ __device__ void mma_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint3
             mma_ts(d_tmem, a_tmem + kk * 8, bdesc + ((kk * 16 * 128) >> 4), kIdescPV,
                    (accumulate || kk > 0) ? 1u : 0u);
     };
+    // S_i(j) with its signals (j = the K/V block of the score tile).
+    auto qk_group = [&](int i, uint32_t kslot, int j, const Task& tk) {
+        if (elect_one_sync()) {
+            issue_qk(i, kslot);
+            mma_commit(&bars.s_full[i]);
+            if (j == tk.nb[i] - 1) mma_commit(&bars.q_empty[i]);
+        }
+        __syncwarp();
+    };
 
-    for (int t = blockIdx.x; t < a.num_tasks && ok; t += gridDim.x) {
+    for (int t = blockIdx.x; t < a.num_tasks; t += gridDim.x) {
         const Task tk = decode_task<CAUSAL>(t, a);
         uint32_t kslot, vslot;
-        wait_slot(kslot);  // K_0
-        if (!ok) break;
-        for (int i = 0; i < 2 && ok; ++i) {
-            if (tk.nb[i] == 0) continue;
-            ok = warp_wait(&bars.q_full[i], qcnt[i] & 1u, abort_flag, a.timeout_ns);
-            if (!ok) break;
-            tc_fence_after();
-            if (elect_one_sync()) {
-                issue_qk(i, kslot);
-                mma_commit(&bars.s_full[i]);
-                if (tk.nb[i] == 1) mma_commit(&bars.q_empty[i]);
-            }
-            __syncwarp();
-            if (tk.nb[i] == 1) ++qcnt[i];
+        // Prologue: S_0(0), S_1(0).
+        wait_q(0);
+        wait_kv(kslot);  // K_0
+        if (!sync()) break;
+        if (!HELPER) qk_group(0, kslot, 0, tk);
+        if (tk.nb[0] == 1) ++qcnt[0];
+        if (tk.nb[1] > 0) {
+            wait_q(1);
+            if (!sync()) break;
+            if (!HELPER) qk_group(1, kslot, 0, tk);
+            if (tk.nb[1] == 1) ++qcnt[1];
         }
-        if (!ok) break;
-        if (elect_one_sync()) mma_commit(&bars.kv_empty[kslot]);
-        __syncwarp();
+        if (!HELPER) {
+            if (elect_one_sync()) mma_commit(&bars.kv_empty[kslot]);
+            __syncwarp();
+        }
 
-        // Per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).  A commit costs
-        // the tensor pipe a drain, and adjacent commits drain once, so every
-        // signal except "S_0 ready" is committed together at the end of the
-        // iteration.
-        for (int j = 0; j < tk.nbmax && ok; ++j) {
+        // Per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).  The tensor
+        // core runs one tile's P.V and next scores while the other tile's
+        // softmax works.
+        for (int j = 0; j < tk.nbmax; ++j) {
             const bool has_next = j + 1 < tk.nbmax;
-            // Any barrier test issued right after an MMA group waits for that
-            // group to be taken by the tensor pipe.  With the five-stage ring
-            // a K tile is often still in flight when P_0 is ready, so P.V_0 is
-            // issued first and K_{j+1} waited for after it.
-            wait_slot(vslot);  // V_j
-            if (!ok) break;
-            for (int i = 0; i < 2 && ok; ++i) {
-                if (j < tk.nb[i]) {
-                    ok = warp_wait(&bars.p_full[i], pcnt[i] & 1u, abort_flag, a.timeout_ns);
-                    ++pcnt[i];
-                    if (!ok) break;
-                    tc_fence_after();
+            wait_kv(vslot);  // V_j
+            if (j < tk.nb[0]) wait_p(0);
+            if (!sync()) break;
+            if (!HELPER && j < tk.nb[0]) {
+                if (elect_one_sync()) {
+                    issue_pv(0, vslot, j > 0);
+                    if (j == tk.nb[0] - 1) mma_commit(&bars.o_full[0]);
+                }
+                __syncwarp();
+            }
+            if (has_next) {
+                wait_kv(kslot);  // K_{j+1}
+                if (!sync()) break;
+            }
+            if (j + 1 < tk.nb[0]) {
+                if (!HELPER) qk_group(0, kslot, j + 1, tk);
+                if (j + 1 == tk.nb[0] - 1) ++qcnt[0];
+            }
+            if (j < tk.nb[1]) {
+                wait_p(1);
+                if (!sync()) break;
+                if (!HELPER) {
                     if (elect_one_sync()) {
-                        issue_pv(i, vslot, j > 0);
-                        if (j == tk.nb[i] - 1) mma_commit(&bars.o_full[i]);
+                        issue_pv(1, vslot, j > 0);
+                        if (j == tk.nb[1] - 1) mma_commit(&bars.o_full[1]);
                     }
                     __syncwarp();
                 }
-                if (i == 0 && has_next) {
-                    wait_slot(kslot);  // K_{j+1}
-                    if (!ok) break;
-                }
+            }
+            if (j + 1 < tk.nb[1]) {
+                if (!HELPER) qk_group(1, kslot, j + 1, tk);
+                if (j + 1 == tk.nb[1] - 1) ++qcnt[1];
+            }
+            // V_j and K_{j+1} are released once every MMA issued so far is done.
+            if (!HELPER) {
                 if (elect_one_sync()) {
-                    if (j + 1 < tk.nb[i]) {
-                        issue_qk(i, kslot);
-                        mma_commit(&bars.s_full[i]);
-                        if (j + 1 == tk.nb[i] - 1) mma_commit(&bars.q_empty[i]);
-                    }
+                    mma_commit(&bars.kv_empty[vslot]);
+                    if (has_next) mma_commit(&bars.kv_empty[kslot]);
                 }
                 __syncwarp();
-                if (j + 1 < tk.nb[i] && j + 1 == tk.nb[i] - 1) ++qcnt[i];
             }
-            if (!ok) break;
-            // V_j and K_{j+1} are released once every MMA issued so far is done.
-            if (elect_one_sync()) {
-                mma_commit(&bars.kv_empty[vslot]);
-                if (has_next) mma_commit(&bars.kv_empty[kslot]);
-            }
-            __syncwarp();
         }
+        if (!ok) break;
     }
 
-    // Drain: every MMA issued above has completed before TMEM is released.
-    if (elect_one_sync()) mma_commit(bars.drain);
-    __syncwarp();
-    warp_wait(bars.drain, 0u, nullptr, a.timeout_ns);
+    if (!HELPER) {
+        // Drain: every MMA issued above has completed before TMEM is released.
+        if (elect_one_sync()) mma_commit(bars.drain);
+        __syncwarp();
+        warp_wait(bars.drain, 0u, nullptr, a.timeout_ns);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -796,7 +834,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid
             if constexpr (L::kRot)
                 mma_role_rot<BF16, CAUSAL>(a, smem, bars, tmem_base, abort_flag);
             else
-                mma_role<D, BF16, CAUSAL>(a, smem, bars, tmem_base, abort_flag);
+                mma_pair_role<D, BF16, CAUSAL, false>(a, smem, bars, tmem_base, abort_flag);
+        } else if (warp == 10) {
+            if constexpr (!L::kRot) mma_pair_role<D, BF16, CAUSAL, true>(a, smem, bars, tmem_base, abort_flag);
         } else if (warp == 9) {
             producer_role<D, CAUSAL>(a, smem, bars, abort_flag);
         }

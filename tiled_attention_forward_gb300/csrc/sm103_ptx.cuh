@@ -329,6 +329,22 @@ __device__ __forceinline__ bool elect_one_sync() {
     return pred != 0u;
 }
 
+// Named barrier `id` over `nthreads` threads (whole warps), with an AND
+// reduction: every participant gets true iff every participant passed true.
+// A named barrier is not a shared-memory access, so a warp that has just
+// issued tcgen05.mma instructions does not wait behind them to pass it
+// (an mbarrier test there waits until the issued MMAs are taken).
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0u;
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3f(float a, float b, float c) {
     float d;
