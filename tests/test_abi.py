@@ -86,6 +86,10 @@ def test_argument_errors_before_any_cuda_call(lib):
     # byte counts of the overlap checks would overflow int64 otherwise
     assert call_fwd(lib, B=1 << 15, H=1 << 15, N=1 << 30, D=128) == UNSUPPORTED
     assert call_fwd(lib, B=1, H=1 << 20, N=1 << 30, D=64) == UNSUPPORTED
+    # more than 2^30 tensor-core tasks (256-row Q blocks x heads), buffers far
+    # apart so that no overlap check fires first
+    far = dict(q=1 << 20, k=1 << 48, v=1 << 49, o=1 << 50)
+    assert call_fwd(lib, B=1, H=1 << 9, N=1 << 30, D=64, **far) == UNSUPPORTED
 
 
 def test_rowwise_argument_errors(lib):

@@ -315,6 +315,8 @@ int fattn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* l
         return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
     }
 
+    // Task indices (256-row Q blocks x heads) are ints in the kernel.
+    if (ceil_div(N, int64_t(kTcBM) * kTcQTiles) * BH > (int64_t(1) << 30)) return FATTN_ERR_UNSUPPORTED;
     int sms = 0;
     st = current_sm_count(&sms);
     if (st != FATTN_OK) return st;

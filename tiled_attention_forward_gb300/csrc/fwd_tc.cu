@@ -21,8 +21,8 @@
 //              O_i += P_i V_j (TS form), tcgen05.commit -> mbarriers
 //   warp 9     TMA producer (one elected lane): Q tiles once per task, K/V tiles
 //              through a ring of shared-memory stages
-//   warp 10    D = 128: the MMA warp's helper, which does the MMA warp's
-//              barrier waits and releases it on a named barrier
+//   warp 10    the MMA warp's helper: does the MMA warp's barrier waits and
+//              releases it on a named barrier
 //   warp 11    idle
 // The control warpgroup (warps 8-11) gives up registers (setmaxnreg) so the
 // softmax warpgroups can hold a whole 128-score row per thread: 168 per
@@ -42,7 +42,7 @@
 // That is the D = 128 layout.  At D = 64 the TMEM has room for a third S
 // buffer, and the two tiles rotate through three buffers so that a tile's
 // next scores are computed while its softmax still works on the current
-// ones (mma_role_rot below; softmax_role serves both layouts).
+// ones (mma_pair_role_rot below; softmax_role serves both layouts).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -100,7 +100,7 @@ struct Task {
 // Task order: non-causal, head-major (all Q blocks of one head are adjacent so
 // concurrently running CTAs share that head's K/V in L2).  Causal, longest
 // first: Q blocks nearest the end of the sequence (most K/V tiles) are
-// scheduled first, heads inner.
+// scheduled first, heads inner; task_of() deals them out.
 template <bool CAUSAL, bool EQUAL = false>
 __device__ __forceinline__ Task decode_task(int t, const TcArgs& a) {
     Task k;
@@ -135,6 +135,16 @@ __device__ __forceinline__ Task decode_task(int t, const TcArgs& a) {
         k.nb[1] = k.nbmax;
     }
     return k;
+}
+
+// The k-th task of this CTA.  Tasks are dealt in waves of gridDim.x, every
+// other wave in reverse CTA order (a snake), so that with the causal order
+// (longest first) each CTA's total work comes out nearly the same; a plain
+// stride gives CTA 0 the longest task of every wave.
+__device__ __forceinline__ int task_of(int k) {
+    const int g = static_cast<int>(gridDim.x);
+    const int c = (k & 1) ? g - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+    return k * g + c;
 }
 
 struct Bars {
@@ -228,7 +238,9 @@ __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
         ++kv_it;
     };
 
-    for (int t = blockIdx.x; t < a.num_tasks && ok; t += gridDim.x) {
+    for (int kt = 0; ok; ++kt) {
+        const int t = task_of(kt);
+        if (t >= a.num_tasks) break;
         const Task tk = decode_task<CAUSAL, L::kRot>(t, a);
         const int kvh = kv_head_of(tk.bh, a.H, a.Hkv);
         load_q(0, tk);
@@ -348,7 +360,9 @@ __device__ void mma_pair_role(const TcArgs& a, uint8_t* smem, const Bars& bars, 
         __syncwarp();
     };
 
-    for (int t = blockIdx.x; t < a.num_tasks; t += gridDim.x) {
+    for (int kt = 0;; ++kt) {
+        const int t = task_of(kt);
+        if (t >= a.num_tasks) break;
         const Task tk = decode_task<CAUSAL>(t, a);
         uint32_t kslot, vslot;
         // Prologue: S_0(0), S_1(0).
@@ -448,9 +462,11 @@ __device__ void mma_pair_role(const TcArgs& a, uint8_t* smem, const Bars& bars, 
 // s_full[b * 2 + i] has one waiting warpgroup (tile i), which sees every phase;
 // the MMA warp waits for P in product order on p_full[b].
 
-template <bool BF16, bool CAUSAL>
-__device__ void mma_role_rot(const TcArgs& a, uint8_t* smem, const Bars& bars, uint32_t tmem_base,
-                             volatile uint32_t* abort_flag) {
+template <bool BF16, bool CAUSAL, bool HELPER>
+__device__ void mma_pair_role_rot(const TcArgs& a, uint8_t* smem, const Bars& bars, uint32_t tmem_base,
+                                  volatile uint32_t* abort_flag) {
+    // Issuing warp and helper warp as in mma_pair_role: the helper does every
+    // mbarrier wait and meets the issuing warp on the named barrier kMmaSync.
     constexpr int D = 64;
     using L = TcLayout<D>;
     constexpr uint32_t kIdescQK = idesc_f16_f32(kTcBM, kTcBN, BF16 ? 1u : 0u, 0u, 0u);
@@ -465,11 +481,23 @@ __device__ void mma_role_rot(const TcArgs& a, uint8_t* smem, const Bars& bars, u
     uint32_t qcnt = 0;     // tasks started (q_full phases of both tiles)
     bool ok = true;
 
+    // Ring slot of a position; the helper also waits for it to be filled.
     auto wait_pos = [&](uint32_t pos) -> uint32_t {
         const uint32_t slot = pos % L::kStages;
-        ok = warp_wait(&bars.kv_full[slot], (pos / L::kStages) & 1u, abort_flag, a.timeout_ns);
-        tc_fence_after();
+        if (HELPER && ok)
+            ok = warp_wait(&bars.kv_full[slot], (pos / L::kStages) & 1u, abort_flag, a.timeout_ns);
         return slot;
+    };
+    auto wait_q = [&](int i) {
+        if (HELPER && ok) ok = warp_wait(&bars.q_full[i], qcnt & 1u, abort_flag, a.timeout_ns);
+    };
+    auto wait_p = [&](uint32_t k) {
+        if (HELPER && ok) ok = warp_wait(&bars.p_full[k % 3u], (k / 3u) & 1u, abort_flag, a.timeout_ns);
+    };
+    auto sync = [&]() -> bool {
+        ok = named_barrier_and(kMmaSync, kMmaSyncThreads, ok);
+        if (!HELPER) tc_fence_after();
+        return ok;
     };
     // S product into buffer b: Q tile i against the K tile in ring slot ks.
     auto issue_s = [&](uint32_t b, int i, uint32_t ks) {
@@ -490,86 +518,96 @@ __device__ void mma_role_rot(const TcArgs& a, uint8_t* smem, const Bars& bars, u
                    bdesc + ((kk * 16 * 128) >> 4), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
         mma_commit(&bars.o_ready[i]);
     };
-    auto wait_p = [&](uint32_t k) {
-        ok = warp_wait(&bars.p_full[k % 3u], (k / 3u) & 1u, abort_flag, a.timeout_ns);
-        tc_fence_after();
-    };
 
-    for (int t = blockIdx.x; t < a.num_tasks && ok; t += gridDim.x) {
+    for (int kt = 0;; ++kt) {
+        const int t = task_of(kt);
+        if (t >= a.num_tasks) break;
         const Task tk = decode_task<CAUSAL, true>(t, a);
         const int nb = tk.nbmax;
         // Prologue: S_0(0), S_1(0), S_0(1).
-        ok = warp_wait(&bars.q_full[0], qcnt & 1u, abort_flag, a.timeout_ns);
-        if (!ok) break;
-        uint32_t ks = wait_pos(kv_base);
-        if (!ok) break;
-        if (elect_one_sync()) {
-            issue_s(sbase % 3u, 0, ks);
-            if (nb == 1) mma_commit(&bars.q_empty[0]);
+        wait_q(0);
+        const uint32_t ks = wait_pos(kv_base);
+        if (!sync()) break;
+        if (!HELPER) {
+            if (elect_one_sync()) {
+                issue_s(sbase % 3u, 0, ks);
+                if (nb == 1) mma_commit(&bars.q_empty[0]);
+            }
+            __syncwarp();
         }
-        __syncwarp();
-        ok = warp_wait(&bars.q_full[1], qcnt & 1u, abort_flag, a.timeout_ns);
-        if (!ok) break;
-        tc_fence_after();
-        if (elect_one_sync()) {
-            issue_s((sbase + 1u) % 3u, 1, ks);
-            mma_commit(&bars.kv_empty[ks]);
-            if (nb == 1) mma_commit(&bars.q_empty[1]);
+        wait_q(1);
+        if (!sync()) break;
+        if (!HELPER) {
+            if (elect_one_sync()) {
+                issue_s((sbase + 1u) % 3u, 1, ks);
+                mma_commit(&bars.kv_empty[ks]);
+                if (nb == 1) mma_commit(&bars.q_empty[1]);
+            }
+            __syncwarp();
         }
-        __syncwarp();
         uint32_t ks_next = 0;  // ring slot of K_{j+1}
         if (nb > 1) {
             ks_next = wait_pos(kv_base + 2u);
-            if (!ok) break;
-            if (elect_one_sync()) {
-                issue_s((sbase + 2u) % 3u, 0, ks_next);
-                if (nb == 2) mma_commit(&bars.q_empty[0]);
-            }
-            __syncwarp();
-        }
-        for (int j = 0; j < nb && ok; ++j) {
-            const uint32_t k0 = sbase + 2u * j;
-            const uint32_t vs = wait_pos(kv_base + 2u * j + 1u);  // V_j
-            if (!ok) break;
-            wait_p(k0);
-            if (!ok) break;
-            if (elect_one_sync()) {
-                issue_pv(k0 % 3u, 0, vs, j > 0);
-                if (j == nb - 1) mma_commit(&bars.o_full[0]);
-                if (j + 1 < nb) {  // S_1(j+1) into the buffer P_0(j) leaves
-                    issue_s(k0 % 3u, 1, ks_next);
-                    mma_commit(&bars.kv_empty[ks_next]);
-                    if (j + 1 == nb - 1) mma_commit(&bars.q_empty[1]);
-                }
-            }
-            __syncwarp();
-            wait_p(k0 + 1u);
-            if (!ok) break;
-            if (elect_one_sync()) {
-                issue_pv((k0 + 1u) % 3u, 1, vs, j > 0);
-                if (j == nb - 1) mma_commit(&bars.o_full[1]);
-                mma_commit(&bars.kv_empty[vs]);
-            }
-            __syncwarp();
-            if (j + 2 < nb) {  // S_0(j+2) into the buffer P_1(j) leaves
-                ks_next = wait_pos(kv_base + 2u * (j + 2));
-                if (!ok) break;
+            if (!sync()) break;
+            if (!HELPER) {
                 if (elect_one_sync()) {
-                    issue_s((k0 + 1u) % 3u, 0, ks_next);
-                    if (j + 2 == nb - 1) mma_commit(&bars.q_empty[0]);
+                    issue_s((sbase + 2u) % 3u, 0, ks_next);
+                    if (nb == 2) mma_commit(&bars.q_empty[0]);
                 }
                 __syncwarp();
             }
         }
+        for (int j = 0; j < nb; ++j) {
+            const uint32_t k0 = sbase + 2u * j;
+            const uint32_t vs = wait_pos(kv_base + 2u * j + 1u);  // V_j
+            wait_p(k0);
+            if (!sync()) break;
+            if (!HELPER) {
+                if (elect_one_sync()) {
+                    issue_pv(k0 % 3u, 0, vs, j > 0);
+                    if (j == nb - 1) mma_commit(&bars.o_full[0]);
+                    if (j + 1 < nb) {  // S_1(j+1) into the buffer P_0(j) leaves
+                        issue_s(k0 % 3u, 1, ks_next);
+                        mma_commit(&bars.kv_empty[ks_next]);
+                        if (j + 1 == nb - 1) mma_commit(&bars.q_empty[1]);
+                    }
+                }
+                __syncwarp();
+            }
+            wait_p(k0 + 1u);
+            if (!sync()) break;
+            if (!HELPER) {
+                if (elect_one_sync()) {
+                    issue_pv((k0 + 1u) % 3u, 1, vs, j > 0);
+                    if (j == nb - 1) mma_commit(&bars.o_full[1]);
+                    mma_commit(&bars.kv_empty[vs]);
+                }
+                __syncwarp();
+            }
+            if (j + 2 < nb) {  // S_0(j+2) into the buffer P_1(j) leaves
+                ks_next = wait_pos(kv_base + 2u * (j + 2));
+                if (!sync()) break;
+                if (!HELPER) {
+                    if (elect_one_sync()) {
+                        issue_s((k0 + 1u) % 3u, 0, ks_next);
+                        if (j + 2 == nb - 1) mma_commit(&bars.q_empty[0]);
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+        if (!ok) break;
         kv_base += 2u * nb;
         sbase += 2u * nb;
         ++qcnt;
     }
 
-    // Drain: every MMA issued above has completed before TMEM is released.
-    if (elect_one_sync()) mma_commit(bars.drain);
-    __syncwarp();
-    warp_wait(bars.drain, 0u, nullptr, a.timeout_ns);
+    if (!HELPER) {
+        // Drain: every MMA issued above has completed before TMEM is released.
+        if (elect_one_sync()) mma_commit(bars.drain);
+        __syncwarp();
+        warp_wait(bars.drain, 0u, nullptr, a.timeout_ns);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -592,7 +630,9 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
     uint32_t ocnt = 0;     // tasks of this tile (o_full phases)
     uint32_t pv_base = 0;  // D = 64: P.V products of this tile in earlier tasks
     uint32_t sbase = 0;    // D = 64: S products of both tiles in earlier tasks
-    for (int t = blockIdx.x; t < a.num_tasks; t += gridDim.x) {
+    for (int kt = 0;; ++kt) {
+        const int t = task_of(kt);
+        if (t >= a.num_tasks) break;
         const Task tk = decode_task<CAUSAL, kRot>(t, a);
         const int nb = tk.nb[tile];
         if constexpr (!kRot) {
@@ -830,13 +870,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid
         softmax_role<D, BF16, CAUSAL>(a, bars, tmem_base, abort_flag);
     } else {
         regs_decrease<kControlRegs>();
-        if (warp == 8) {
-            if constexpr (L::kRot)
-                mma_role_rot<BF16, CAUSAL>(a, smem, bars, tmem_base, abort_flag);
-            else
-                mma_pair_role<D, BF16, CAUSAL, false>(a, smem, bars, tmem_base, abort_flag);
-        } else if (warp == 10) {
-            if constexpr (!L::kRot) mma_pair_role<D, BF16, CAUSAL, true>(a, smem, bars, tmem_base, abort_flag);
+        if (warp == 8 || warp == 10) {  // the issuing warp and its helper
+            if constexpr (L::kRot) {
+                if (warp == 8)
+                    mma_pair_role_rot<BF16, CAUSAL, false>(a, smem, bars, tmem_base, abort_flag);
+                else
+                    mma_pair_role_rot<BF16, CAUSAL, true>(a, smem, bars, tmem_base, abort_flag);
+            } else {
+                if (warp == 8)
+                    mma_pair_role<D, BF16, CAUSAL, false>(a, smem, bars, tmem_base, abort_flag);
+                else
+                    mma_pair_role<D, BF16, CAUSAL, true>(a, smem, bars, tmem_base, abort_flag);
+            }
         } else if (warp == 9) {
             producer_role<D, CAUSAL>(a, smem, bars, abort_flag);
         }
