@@ -73,12 +73,12 @@ struct TcLayout {
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = kTcQTiles * kQTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kKVTileBytes;
-    // D = 128: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] drain[1]
-    // D = 64 (three S buffers): ... s_full[3][2] p_full[3] o_full[2] o_ready[2] drain[1]
+    // D = 128: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] o_full[2] drain[1]
+    // D = 64 (three S buffers): ... s_full[3][2] o_full[2] o_ready[2] drain[1]
+    // (P is handed to the MMA warp on named barriers, see kPBar.)
     static constexpr bool kRot = (D == 64);
     static constexpr int kSFull = kRot ? 6 : 2;
-    static constexpr int kPFull = kRot ? 3 : 2;
-    static constexpr int kNumBars = 2 + 2 + 2 * kStages + kSFull + kPFull + 2 + (kRot ? 2 : 0) + 1;
+    static constexpr int kNumBars = 2 + 2 + 2 * kStages + kSFull + 2 + (kRot ? 2 : 0) + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kAlloc = kBytes;  // the dynamic base is declared 1024-byte aligned
@@ -153,7 +153,6 @@ struct Bars {
     uint64_t* kv_full;
     uint64_t* kv_empty;
     uint64_t* s_full;
-    uint64_t* p_full;  // D = 128: [tile]; D = 64: [S buffer]: P stored (and O rescaled)
     uint64_t* o_full;
     uint64_t* o_ready;  // D = 64: [tile], one phase per completed P.V product
     uint64_t* drain;
@@ -169,8 +168,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
     r.kv_full = b + 4;
     r.kv_empty = r.kv_full + L::kStages;
     r.s_full = r.kv_empty + L::kStages;
-    r.p_full = r.s_full + L::kSFull;
-    r.o_full = r.p_full + L::kPFull;
+    r.o_full = r.s_full + L::kSFull;
     r.o_ready = r.o_full + 2;
     r.drain = r.o_ready + (L::kRot ? 2 : 0);
     return r;
@@ -280,6 +278,22 @@ __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
 // warps leave the schedule at the same point when a wait gives up.
 constexpr uint32_t kMmaSync = 1;          // named barrier id (0 is __syncthreads)
 constexpr uint32_t kMmaSyncThreads = 64;  // the issuing warp and its helper
+// P of Q tile i, K/V block j is handed from softmax warpgroup i to the
+// issuing warp on named barrier kPBar + 2 i + (j & 1): the warpgroup arrives
+// (no wait), the issuing warp waits.  A warpgroup can finish the P of the
+// next block before the issuing warp has taken the current one (its next
+// scores may already be computed), never the one after, so two barriers per
+// tile alternate.  Ids 2..5.
+constexpr uint32_t kPBar = 2;
+constexpr uint32_t kPBarThreads = 128 + 32;  // one softmax warpgroup and the issuing warp
+
+// Every wait on a named barrier is unbounded, so on an abort (an mbarrier
+// wait that gave up) no role leaves early: each runs the rest of its
+// schedule "dry" -- no mbarrier waits, MMAs, TMEM traffic or stores -- and
+// still passes every named barrier, so that every named-barrier wait is met.
+__device__ __forceinline__ uint32_t p_bar(int tile, int j) {
+    return kPBar + 2u * static_cast<uint32_t>(tile) + (static_cast<uint32_t>(j) & 1u);
+}
 
 template <int D, bool BF16, bool CAUSAL, bool HELPER>
 __device__ void mma_pair_role(const TcArgs& a, uint8_t* smem, const Bars& bars, uint32_t tmem_base,
@@ -293,8 +307,7 @@ __device__ void mma_pair_role(const TcArgs& a, uint8_t* smem, const Bars& bars, 
 
     uint32_t kv_it = 0;               // ring positions consumed (both warps count alike)
     uint32_t qcnt[2] = {0u, 0u};
-    uint32_t pcnt[2] = {0u, 0u};
-    bool ok = true;
+    bool ok = true;                   // false: dry run (see kPBar)
 
     // The helper's waits; the issuing warp only advances the same counters.
     auto wait_kv = [&](uint32_t& slot) {
@@ -306,15 +319,18 @@ __device__ void mma_pair_role(const TcArgs& a, uint8_t* smem, const Bars& bars, 
     auto wait_q = [&](int i) {
         if (HELPER && ok) ok = warp_wait(&bars.q_full[i], qcnt[i] & 1u, abort_flag, a.timeout_ns);
     };
-    auto wait_p = [&](int i) {
-        if (HELPER && ok) ok = warp_wait(&bars.p_full[i], pcnt[i] & 1u, abort_flag, a.timeout_ns);
-        ++pcnt[i];
-    };
-    // Both warps pass here together; false when a wait of the helper gave up.
-    auto sync = [&]() -> bool {
+    // Both warps pass here together; false (from then on) once a wait of the
+    // helper gave up.
+    auto sync = [&]() {
         ok = named_barrier_and(kMmaSync, kMmaSyncThreads, ok);
         if (!HELPER) tc_fence_after();
-        return ok;
+    };
+    // The issuing warp takes P of tile i, block j from its softmax warpgroup.
+    auto take_p = [&](int i, int j) {
+        if (!HELPER) {
+            named_barrier_sync(p_bar(i, j), kPBarThreads);
+            tc_fence_after();
+        }
     };
 
     // Descriptor templates with a zero start address.  A tile's descriptor is
@@ -352,12 +368,23 @@ __device__ void mma_pair_role(const TcArgs& a, uint8_t* smem, const Bars& bars, 
     };
     // S_i(j) with its signals (j = the K/V block of the score tile).
     auto qk_group = [&](int i, uint32_t kslot, int j, const Task& tk) {
-        if (elect_one_sync()) {
-            issue_qk(i, kslot);
-            mma_commit(&bars.s_full[i]);
-            if (j == tk.nb[i] - 1) mma_commit(&bars.q_empty[i]);
+        if (!HELPER && ok) {
+            if (elect_one_sync()) {
+                issue_qk(i, kslot);
+                mma_commit(&bars.s_full[i]);
+                if (j == tk.nb[i] - 1) mma_commit(&bars.q_empty[i]);
+            }
+            __syncwarp();
         }
-        __syncwarp();
+    };
+    auto pv_group = [&](int i, uint32_t vslot, int j, const Task& tk) {
+        if (!HELPER && ok) {
+            if (elect_one_sync()) {
+                issue_pv(i, vslot, j > 0);
+                if (j == tk.nb[i] - 1) mma_commit(&bars.o_full[i]);
+            }
+            __syncwarp();
+        }
     };
 
     for (int kt = 0;; ++kt) {
@@ -368,60 +395,47 @@ __device__ void mma_pair_role(const TcArgs& a, uint8_t* smem, const Bars& bars, 
         // Prologue: S_0(0), S_1(0).
         wait_q(0);
         wait_kv(kslot);  // K_0
-        if (!sync()) break;
-        if (!HELPER) qk_group(0, kslot, 0, tk);
+        sync();
+        qk_group(0, kslot, 0, tk);
         if (tk.nb[0] == 1) ++qcnt[0];
         if (tk.nb[1] > 0) {
             wait_q(1);
-            if (!sync()) break;
-            if (!HELPER) qk_group(1, kslot, 0, tk);
+            sync();
+            qk_group(1, kslot, 0, tk);
             if (tk.nb[1] == 1) ++qcnt[1];
         }
-        if (!HELPER) {
+        if (!HELPER && ok) {
             if (elect_one_sync()) mma_commit(&bars.kv_empty[kslot]);
             __syncwarp();
         }
 
         // Per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).  The tensor
         // core runs one tile's P.V and next scores while the other tile's
-        // softmax works.
+        // softmax works.  V_j and K_{j+1} are waited for together: K_{j+1}
+        // lands right after V_j, and one meeting per block is cheaper.
         for (int j = 0; j < tk.nbmax; ++j) {
             const bool has_next = j + 1 < tk.nbmax;
-            wait_kv(vslot);  // V_j
-            if (j < tk.nb[0]) wait_p(0);
-            if (!sync()) break;
-            if (!HELPER && j < tk.nb[0]) {
-                if (elect_one_sync()) {
-                    issue_pv(0, vslot, j > 0);
-                    if (j == tk.nb[0] - 1) mma_commit(&bars.o_full[0]);
-                }
-                __syncwarp();
-            }
-            if (has_next) {
-                wait_kv(kslot);  // K_{j+1}
-                if (!sync()) break;
+            wait_kv(vslot);                  // V_j
+            if (has_next) wait_kv(kslot);    // K_{j+1}
+            sync();
+            if (j < tk.nb[0]) {
+                take_p(0, j);
+                pv_group(0, vslot, j, tk);
             }
             if (j + 1 < tk.nb[0]) {
-                if (!HELPER) qk_group(0, kslot, j + 1, tk);
+                qk_group(0, kslot, j + 1, tk);
                 if (j + 1 == tk.nb[0] - 1) ++qcnt[0];
             }
             if (j < tk.nb[1]) {
-                wait_p(1);
-                if (!sync()) break;
-                if (!HELPER) {
-                    if (elect_one_sync()) {
-                        issue_pv(1, vslot, j > 0);
-                        if (j == tk.nb[1] - 1) mma_commit(&bars.o_full[1]);
-                    }
-                    __syncwarp();
-                }
+                take_p(1, j);
+                pv_group(1, vslot, j, tk);
             }
             if (j + 1 < tk.nb[1]) {
-                if (!HELPER) qk_group(1, kslot, j + 1, tk);
+                qk_group(1, kslot, j + 1, tk);
                 if (j + 1 == tk.nb[1] - 1) ++qcnt[1];
             }
             // V_j and K_{j+1} are released once every MMA issued so far is done.
-            if (!HELPER) {
+            if (!HELPER && ok) {
                 if (elect_one_sync()) {
                     mma_commit(&bars.kv_empty[vslot]);
                     if (has_next) mma_commit(&bars.kv_empty[kslot]);
@@ -429,7 +443,6 @@ __device__ void mma_pair_role(const TcArgs& a, uint8_t* smem, const Bars& bars, 
                 __syncwarp();
             }
         }
-        if (!ok) break;
     }
 
     if (!HELPER) {
@@ -460,13 +473,14 @@ __device__ void mma_pair_role(const TcArgs& a, uint8_t* smem, const Bars& bars, 
 // warpgroup sees S_i(j) complete, P.V_i(j-2) is complete too, and its wait
 // for P.V_i(j-1) on o_ready[i] (only to rescale O_i) is never two phases away;
 // s_full[b * 2 + i] has one waiting warpgroup (tile i), which sees every phase;
-// the MMA warp waits for P in product order on p_full[b].
+// the MMA warp takes P in product order on the kPBar named barriers.
 
 template <bool BF16, bool CAUSAL, bool HELPER>
 __device__ void mma_pair_role_rot(const TcArgs& a, uint8_t* smem, const Bars& bars, uint32_t tmem_base,
                                   volatile uint32_t* abort_flag) {
     // Issuing warp and helper warp as in mma_pair_role: the helper does every
-    // mbarrier wait and meets the issuing warp on the named barrier kMmaSync.
+    // mbarrier wait and meets the issuing warp on the named barrier kMmaSync;
+    // P comes from the softmax warpgroups on the kPBar named barriers.
     constexpr int D = 64;
     using L = TcLayout<D>;
     constexpr uint32_t kIdescQK = idesc_f16_f32(kTcBM, kTcBN, BF16 ? 1u : 0u, 0u, 0u);
@@ -479,7 +493,7 @@ __device__ void mma_pair_role_rot(const TcArgs& a, uint8_t* smem, const Bars& ba
     uint32_t kv_base = 0;  // ring position of the task's K_0 (K_j at 2j, V_j at 2j + 1)
     uint32_t sbase = 0;    // products of earlier tasks
     uint32_t qcnt = 0;     // tasks started (q_full phases of both tiles)
-    bool ok = true;
+    bool ok = true;        // false: dry run (see kPBar)
 
     // Ring slot of a position; the helper also waits for it to be filled.
     auto wait_pos = [&](uint32_t pos) -> uint32_t {
@@ -491,14 +505,17 @@ __device__ void mma_pair_role_rot(const TcArgs& a, uint8_t* smem, const Bars& ba
     auto wait_q = [&](int i) {
         if (HELPER && ok) ok = warp_wait(&bars.q_full[i], qcnt & 1u, abort_flag, a.timeout_ns);
     };
-    auto wait_p = [&](uint32_t k) {
-        if (HELPER && ok) ok = warp_wait(&bars.p_full[k % 3u], (k / 3u) & 1u, abort_flag, a.timeout_ns);
-    };
-    auto sync = [&]() -> bool {
+    auto sync = [&]() {
         ok = named_barrier_and(kMmaSync, kMmaSyncThreads, ok);
         if (!HELPER) tc_fence_after();
-        return ok;
     };
+    auto take_p = [&](int i, int j) {
+        if (!HELPER) {
+            named_barrier_sync(p_bar(i, j), kPBarThreads);
+            tc_fence_after();
+        }
+    };
+    const bool issuer = !HELPER;
     // S product into buffer b: Q tile i against the K tile in ring slot ks.
     auto issue_s = [&](uint32_t b, int i, uint32_t ks) {
         const uint64_t adesc = kmaj_desc + ((q_smem + i * L::kQTileBytes) >> 4);
@@ -526,43 +543,33 @@ __device__ void mma_pair_role_rot(const TcArgs& a, uint8_t* smem, const Bars& ba
         const int nb = tk.nbmax;
         // Prologue: S_0(0), S_1(0), S_0(1).
         wait_q(0);
+        wait_q(1);
         const uint32_t ks = wait_pos(kv_base);
-        if (!sync()) break;
-        if (!HELPER) {
+        uint32_t ks_next = 0;  // ring slot of K_{j+1}
+        if (nb > 1) ks_next = wait_pos(kv_base + 2u);
+        sync();
+        if (issuer && ok) {
             if (elect_one_sync()) {
                 issue_s(sbase % 3u, 0, ks);
                 if (nb == 1) mma_commit(&bars.q_empty[0]);
-            }
-            __syncwarp();
-        }
-        wait_q(1);
-        if (!sync()) break;
-        if (!HELPER) {
-            if (elect_one_sync()) {
                 issue_s((sbase + 1u) % 3u, 1, ks);
                 mma_commit(&bars.kv_empty[ks]);
                 if (nb == 1) mma_commit(&bars.q_empty[1]);
-            }
-            __syncwarp();
-        }
-        uint32_t ks_next = 0;  // ring slot of K_{j+1}
-        if (nb > 1) {
-            ks_next = wait_pos(kv_base + 2u);
-            if (!sync()) break;
-            if (!HELPER) {
-                if (elect_one_sync()) {
+                if (nb > 1) {
                     issue_s((sbase + 2u) % 3u, 0, ks_next);
                     if (nb == 2) mma_commit(&bars.q_empty[0]);
                 }
-                __syncwarp();
             }
+            __syncwarp();
         }
         for (int j = 0; j < nb; ++j) {
             const uint32_t k0 = sbase + 2u * j;
             const uint32_t vs = wait_pos(kv_base + 2u * j + 1u);  // V_j
-            wait_p(k0);
-            if (!sync()) break;
-            if (!HELPER) {
+            uint32_t ks2 = 0;                                     // K_{j+2}
+            if (j + 2 < nb) ks2 = wait_pos(kv_base + 2u * (j + 2));
+            sync();
+            take_p(0, j);
+            if (issuer && ok) {
                 if (elect_one_sync()) {
                     issue_pv(k0 % 3u, 0, vs, j > 0);
                     if (j == nb - 1) mma_commit(&bars.o_full[0]);
@@ -574,29 +581,21 @@ __device__ void mma_pair_role_rot(const TcArgs& a, uint8_t* smem, const Bars& ba
                 }
                 __syncwarp();
             }
-            wait_p(k0 + 1u);
-            if (!sync()) break;
-            if (!HELPER) {
+            take_p(1, j);
+            if (issuer && ok) {
                 if (elect_one_sync()) {
                     issue_pv((k0 + 1u) % 3u, 1, vs, j > 0);
                     if (j == nb - 1) mma_commit(&bars.o_full[1]);
                     mma_commit(&bars.kv_empty[vs]);
+                    if (j + 2 < nb) {  // S_0(j+2) into the buffer P_1(j) leaves
+                        issue_s((k0 + 1u) % 3u, 0, ks2);
+                        if (j + 2 == nb - 1) mma_commit(&bars.q_empty[0]);
+                    }
                 }
                 __syncwarp();
             }
-            if (j + 2 < nb) {  // S_0(j+2) into the buffer P_1(j) leaves
-                ks_next = wait_pos(kv_base + 2u * (j + 2));
-                if (!sync()) break;
-                if (!HELPER) {
-                    if (elect_one_sync()) {
-                        issue_s((k0 + 1u) % 3u, 0, ks_next);
-                        if (j + 2 == nb - 1) mma_commit(&bars.q_empty[0]);
-                    }
-                    __syncwarp();
-                }
-            }
+            if (j + 2 < nb) ks_next = ks2;
         }
-        if (!ok) break;
         kv_base += 2u * nb;
         sbase += 2u * nb;
         ++qcnt;
@@ -613,6 +612,23 @@ __device__ void mma_pair_role_rot(const TcArgs& a, uint8_t* smem, const Bars& ba
 // ---------------------------------------------------------------------------
 // Softmax + correction + epilogue (one warpgroup per Q tile), both layouts
 // ---------------------------------------------------------------------------
+// After a wait of a softmax warpgroup gave up: pass the P named barrier of
+// every block this tile has not handed over yet (block j0 of the CTA's kt0-th
+// task onwards), waiting on nothing, so that the issuing warp, which runs its
+// schedule to the end, meets every barrier it waits on (see kPBar).
+template <bool CAUSAL, bool EQUAL>
+__device__ __noinline__ void softmax_dry_tail(const TcArgs& a, int tile, int kt0, int j0) {
+    for (int kt = kt0;; ++kt) {
+        const int t = task_of(kt);
+        if (t >= a.num_tasks) break;
+        const Task tk = decode_task<CAUSAL, EQUAL>(t, a);
+        for (int j = (kt == kt0) ? j0 : 0; j < tk.nb[tile]; ++j) {
+            __syncwarp();
+            named_barrier_arrive(p_bar(tile, j), kPBarThreads);
+        }
+    }
+}
+
 template <int D, bool BF16, bool CAUSAL>
 __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_base,
                              volatile uint32_t* abort_flag) {
@@ -661,7 +677,10 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
             const uint32_t tS = tmem_base + lane_field + b * kTcBN;
             const bool ok = warp_wait(&bars.s_full[kRot ? b * 2 + tile : b], use & 1u, abort_flag,
                                       a.timeout_ns);
-            if (!ok) return;
+            if (!ok) {
+                softmax_dry_tail<CAUSAL, kRot>(a, tile, kt, j);
+                return;
+            }
             tc_fence_after();
 
             // The whole score row: four 32-column loads in flight, one wait.
@@ -714,8 +733,10 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
                         // O_i holds P.V_i(j-1) only once that product is done
                         // (at D = 128 the commit of S_i(j) already implies it).
                         if (!warp_wait(&bars.o_ready[tile], (pv_base + j - 1) & 1u, abort_flag,
-                                       a.timeout_ns))
+                                       a.timeout_ns)) {
+                            softmax_dry_tail<CAUSAL, kRot>(a, tile, kt, j);
                             return;
+                        }
                         tc_fence_after();
                     }
                     const float alpha = ex2_approx(m_run - m_new);
@@ -758,12 +779,12 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
                 }
                 tmem_st16(tS + c * 16, pk[c]);
             }
-            // P stored: hand it to the MMA warp (one arrival per warp, after
-            // every lane's stores have completed).
+            // P stored: hand it to the issuing warp once every lane's stores
+            // have completed.
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if ((threadIdx.x % 32) == 0) mbar_arrive(&bars.p_full[b]);
+            named_barrier_arrive(p_bar(tile, j), kPBarThreads);
             // The sum of the rounded P (which normalises O) feeds nothing the
             // MMA warp waits for, so it is formed after the hand-off.
             float la[8];
@@ -781,7 +802,10 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
         // Epilogue: O = O~ / l, LSE = (m + log2 l) ln 2, rows < N only.
         const bool ok = warp_wait(&bars.o_full[tile], ocnt & 1u, abort_flag, a.timeout_ns);
         ++ocnt;
-        if (!ok) return;
+        if (!ok) {
+            softmax_dry_tail<CAUSAL, kRot>(a, tile, kt + 1, 0);
+            return;
+        }
         tc_fence_after();
         const float inv_l = 1.f / l_run;
         const bool valid = row < a.N;
@@ -841,8 +865,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid
             if (L::kRot) mbar_init(&bars.o_ready[i], 1);
         }
         for (int b = 0; b < L::kSFull; ++b) mbar_init(&bars.s_full[b], 1);
-        for (int b = 0; b < L::kPFull; ++b)
-            mbar_init(&bars.p_full[b], kTcBM / 32);  // one arrival per softmax warp
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(&bars.kv_full[s], 1);
             mbar_init(&bars.kv_empty[s], 1);

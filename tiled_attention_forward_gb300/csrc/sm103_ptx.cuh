@@ -345,6 +345,16 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t nthreads
     return r != 0u;
 }
 
+// Named barrier `id` over `nthreads` threads: arrive without waiting (whole
+// warp), and arrive-and-wait.  Release / acquire ordering for the threads
+// taking part, like an mbarrier arrive / wait.
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("barrier.cta.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("barrier.cta.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3f(float a, float b, float c) {
     float d;
