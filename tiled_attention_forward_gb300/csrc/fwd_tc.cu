@@ -243,6 +243,20 @@ __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
         const int kvh = kv_head_of(tk.bh, a.H, a.Hkv);
         load_q(0, tk);
         if (!ok) break;
+        // The next task's Q tiles are read once, from DRAM, and their loads
+        // can only start when this task's last score products are done;
+        // fetched into L2 now, they land in shared memory at L2 latency.
+        const int tn = task_of(kt + 1);
+        if (tn < a.num_tasks && elect_one_sync()) {
+            const Task nx = decode_task<CAUSAL, L::kRot>(tn, a);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                if (nx.q0 + i * kTcBM < a.N)
+#pragma unroll
+                    for (int at = 0; at < L::kAtoms; ++at)
+                        tma_prefetch_3d(&a.tmap_q, at * 64, nx.q0 + i * kTcBM, nx.bh);
+        }
+        __syncwarp();
         load_kv(&a.tmap_k, 0, kvh);
         if (!ok) break;
         if (tk.nb[1] > 0) {

@@ -119,6 +119,16 @@ __device__ __forceinline__ void tma_load_3d_hint(void* smem_dst, const CUtensorM
         : "memory");
 }
 
+// Prefetch of one box of a tensor map into L2 (no shared-memory destination,
+// no completion signal).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int32_t c0, int32_t c1,
+                                                int32_t c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // L2 eviction-priority policies for the cache hint above.
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t p;
