@@ -39,8 +39,18 @@ namespace {
 __device__ uint32_t g_error_word;
 
 constexpr int kBT = 128;            // tile edge: rows of every tile, keys / queries per tile
-constexpr int kBwdThreads = 320;    // warps 0-7 elementwise, warp 8 MMA, warp 9 TMA
-constexpr int kMmaWarp = 8, kTmaWarp = 9;
+constexpr int kBwdThreads = 352;    // warps 0-7 elementwise, 8 MMA issue, 9 TMA, 10 MMA helper
+constexpr int kMmaWarp = 8, kTmaWarp = 9, kHelperWarp = 10;
+// Named barriers.  The issuing warp never tests an mbarrier inside its loop
+// (a shared-memory access right after issued MMAs waits until they are
+// taken by the tensor pipe): the helper warp does those waits and meets it on
+// kSyncBar, with an AND of "every wait succeeded"; the elementwise warps hand
+// their 16-bit tiles (kPBar + tile parity: they can run one tile ahead) and,
+// for dQ, the dP columns they have read (kDpBar) over named barriers too.
+constexpr uint32_t kSyncBar = 1, kSyncThreads = 64;
+constexpr uint32_t kPBar = 2;        // 2, 3
+constexpr uint32_t kDpBar = 4;
+constexpr uint32_t kEwThreads = 8 * 32 + 32;  // the elementwise warps and the issuing warp
 constexpr uint32_t kTmemCols = 512;
 
 // Shared memory: the two resident tiles, then ring A and ring B.
@@ -68,8 +78,8 @@ struct BwdLayout {
     static constexpr int kRingB = kRingA + kSA * kSlotA;
     static constexpr int kBar = kRingB + kSB * kSlotB;
     // barriers: outer_full, fullA/emptyA[SA], fullB/emptyB[SB], s_full[2],
-    // dp_free, p_full[2], done; abort flag; TMEM slot
-    static constexpr int kBytes = kBar + (7 + 2 * kSA + 2 * kSB) * 8 + 16;
+    // done; abort flag; TMEM slot
+    static constexpr int kBytes = kBar + (4 + 2 * kSA + 2 * kSB) * 8 + 16;
     static_assert(kBytes <= 227 * 1024, "shared memory");
 };
 
@@ -80,8 +90,6 @@ struct BwdBars {
     uint64_t* full_b;
     uint64_t* empty_b;
     uint64_t* s_full;
-    uint64_t* dp_free;
-    uint64_t* p_full;
     uint64_t* done;
     uint32_t* abort_flag;
     uint32_t* tmem_slot;
@@ -98,9 +106,7 @@ __device__ __forceinline__ BwdBars bwd_bars(uint8_t* smem) {
     b.full_b = b.empty_a + L::kSA;
     b.empty_b = b.full_b + L::kSB;
     b.s_full = b.empty_b + L::kSB;   // [2]: one per S buffer / tile parity
-    b.dp_free = b.s_full + 2;
-    b.p_full = b.dp_free + 1;        // [2]
-    b.done = b.p_full + 2;
+    b.done = b.s_full + 2;
     b.abort_flag = reinterpret_cast<uint32_t*>(b.done + 1);
     b.tmem_slot = b.abort_flag + 1;
     return b;
@@ -223,11 +229,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             mbar_init(&bars.full_b[s], 1);
             mbar_init(&bars.empty_b[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars.s_full[i], 1);
-            mbar_init(&bars.p_full[i], 8);
-        }
-        mbar_init(bars.dp_free, 8);
+        for (int i = 0; i < 2; ++i) mbar_init(&bars.s_full[i], 1);
         mbar_init(bars.done, 1);
         *bars.abort_flag = 0u;
         fence_barrier_init();
@@ -328,15 +330,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                 mbar_wait_bounded(bars.outer_full, 0u, nullptr, &g_error_word, a.timeout_ns);
             }
         }
-    } else if (warp == kMmaWarp) {
-        // ---------------- MMA issue (one elected lane) ----------------
-        // dK/dV: S^T and dP^T of 64-query tile it go to TMEM buffer it & 1;
-        // tiles it and it+1 are computed ahead, so while the elementwise warps
-        // work on one buffer the tensor pipe accumulates the previous tile and
-        // fills the other.  dQ: per key tile it, S(it) and dP(it) -> s_full;
-        // the elementwise warps load dP(it) and hand its columns back
-        // (dp_free), so dP(it+1) (and S(it+1), into the other buffer) run
-        // while they work, then dQ += dS K once the 16-bit dS is in TMEM.
+    } else if (warp == kMmaWarp || warp == kHelperWarp) {
+        // ---------------- MMA issue (warp 8) and its helper (warp 10) ----------------
+        // Both warps run the same schedule.  dK/dV: S^T and dP^T of 64-query
+        // tile it go to TMEM buffer it & 1; tiles it and it+1 are computed
+        // ahead, so while the elementwise warps work on one buffer the tensor
+        // pipe accumulates the previous tile and fills the other.  dQ: per
+        // key tile it, S(it) and dP(it) -> s_full; the elementwise warps load
+        // dP(it) and hand its columns back (kDpBar), so dP(it+1) (and
+        // S(it+1), into the other buffer) run while they work, then dQ += dS K
+        // once the 16-bit dS is in TMEM.  On an abort both warps run the rest
+        // of the schedule dry (no waits, no MMAs) and still pass every named
+        // barrier, which the elementwise warps then meet by arriving for
+        // every remaining tile.
+        const bool issuer = warp == kMmaWarp;
         constexpr uint32_t kIdescS = idesc_f16_f32(kBT, KV ? kBQ : kBT, BF16 ? 1u : 0u, 0u, 0u);
         constexpr uint32_t kIdescAcc = idesc_f16_f32(kBT, D, BF16 ? 1u : 0u, 0u, 1u);
         constexpr int kInRows = KV ? kBQ : kBT;
@@ -385,88 +392,100 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                 }
             }
         };
-        // wait for ring A (inner1; for dK/dV the whole slot) / ring B (dQ: V) of tile it
+        bool ok = true;
+        // The helper's waits for ring A (inner1; for dK/dV the whole slot) /
+        // ring B (dQ: V) of tile it.
         auto wait_a = [&](int it) {
-            const bool r = warp_wait(&bars.full_a[it % L::kSA], (it / L::kSA) & 1u, bars.abort_flag,
-                                     a.timeout_ns);
-            tc_fence_after();
-            return r;
+            if (!issuer && ok)
+                ok = warp_wait(&bars.full_a[it % L::kSA], (it / L::kSA) & 1u, bars.abort_flag, a.timeout_ns);
         };
         auto wait_b = [&](int it) {
-            if (KV) return true;
-            const bool r = warp_wait(&bars.full_b[it % L::kSBm], (it / L::kSBm) & 1u, bars.abort_flag,
-                                     a.timeout_ns);
-            tc_fence_after();
-            return r;
+            if (!KV && !issuer && ok)
+                ok = warp_wait(&bars.full_b[it % L::kSBm], (it / L::kSBm) & 1u, bars.abort_flag, a.timeout_ns);
         };
-        bool ok = warp_wait(bars.outer_full, 0u, bars.abort_flag, a.timeout_ns);
+        auto sync = [&]() {
+            ok = named_barrier_and(kSyncBar, kSyncThreads, ok);
+            if (issuer) tc_fence_after();
+        };
+        // The issuing warp takes a tile from the elementwise warps.
+        auto take = [&](uint32_t bar) {
+            if (issuer) {
+                named_barrier_sync(bar, kEwThreads);
+                tc_fence_after();
+            }
+        };
+        // One elected lane of the issuing warp runs f, unless dry.
+        auto issue = [&](auto&& f) {
+            if (issuer && ok) {
+                if (elect_one_sync()) f();
+                __syncwarp();
+            }
+        };
+        if (!issuer && ok) ok = warp_wait(bars.outer_full, 0u, bars.abort_flag, a.timeout_ns);
         if (KV) {
-            for (int t = 0; t < 2 && t < tk.n && ok; ++t) {
-                if (!(ok = wait_a(t))) break;
-                if (elect_one_sync()) {
+            for (int t = 0; t < 2 && t < tk.n; ++t) {
+                wait_a(t);
+                sync();
+                issue([&] {
                     issue_s(t);
                     issue_dp(t);
                     mma_commit(&bars.s_full[t]);
-                }
-                __syncwarp();
+                });
             }
-            for (int it = 0; it < tk.n && ok; ++it) {
-                if (!(ok = warp_wait(&bars.p_full[it & 1], (it >> 1) & 1u, bars.abort_flag, a.timeout_ns))) break;
-                tc_fence_after();
-                if (elect_one_sync()) {
+            for (int it = 0; it < tk.n; ++it) {
+                take(kPBar + (it & 1));
+                issue([&] {
                     issue_acc(it);
                     mma_commit(&bars.empty_a[it % L::kSA]);
-                }
-                __syncwarp();
+                });
                 if (it + 2 < tk.n) {  // tile it+2 into the buffer tile it has just released
-                    if (!(ok = wait_a(it + 2))) break;
-                    if (elect_one_sync()) {
+                    wait_a(it + 2);
+                    sync();
+                    issue([&] {
                         issue_s(it + 2);
                         issue_dp(it + 2);
                         mma_commit(&bars.s_full[it & 1]);
-                    }
-                    __syncwarp();
+                    });
                 }
             }
         } else {
-            if (ok && (ok = wait_a(0) && wait_b(0))) {
-                if (elect_one_sync()) {
-                    issue_s(0);
-                    issue_dp(0);
-                    mma_commit(&bars.s_full[0]);
-                    mma_commit(&bars.empty_b[0]);
-                }
-                __syncwarp();
-            }
-            for (int it = 0; it < tk.n && ok; ++it) {
+            wait_a(0);
+            wait_b(0);
+            sync();
+            issue([&] {
+                issue_s(0);
+                issue_dp(0);
+                mma_commit(&bars.s_full[0]);
+                mma_commit(&bars.empty_b[0]);
+            });
+            for (int it = 0; it < tk.n; ++it) {
                 const bool more = it + 1 < tk.n;
                 if (more) {
-                    if (!(ok = wait_a(it + 1))) break;
-                    if (elect_one_sync()) issue_s(it + 1);
-                    __syncwarp();
+                    wait_a(it + 1);
+                    sync();
+                    issue([&] { issue_s(it + 1); });
                 }
-                if (!(ok = warp_wait(bars.dp_free, it & 1u, bars.abort_flag, a.timeout_ns))) break;
-                tc_fence_after();
+                take(kDpBar);
                 if (more) {
-                    if (!(ok = wait_b(it + 1))) break;
-                    if (elect_one_sync()) {
+                    wait_b(it + 1);
+                    sync();
+                    issue([&] {
                         issue_dp(it + 1);
                         mma_commit(&bars.s_full[(it + 1) & 1]);
                         mma_commit(&bars.empty_b[(it + 1) % L::kSBm]);  // V slot free once dP is done
-                    }
-                    __syncwarp();
+                    });
                 }
-                if (!(ok = warp_wait(&bars.p_full[it & 1], (it >> 1) & 1u, bars.abort_flag, a.timeout_ns))) break;
-                tc_fence_after();
-                if (elect_one_sync()) {
+                take(kPBar + (it & 1));
+                issue([&] {
                     issue_acc(it);
                     mma_commit(&bars.empty_a[it % L::kSA]);
-                }
-                __syncwarp();
+                });
             }
         }
-        if (elect_one_sync()) mma_commit(bars.done);  // fires once every MMA above has completed
-        __syncwarp();
+        if (issuer) {
+            if (elect_one_sync()) mma_commit(bars.done);  // fires once every MMA above has completed
+            __syncwarp();
+        }
     } else {
         // ---------------- elementwise warps 0-7 ----------------
         // Warps w and w+4 share TMEM lane quarter w % 4 (thread = lane =
@@ -485,6 +504,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             ndelta_r = stats[a.Npad];
         }
         bool ok = true;
+        int failed_at = 0;  // first tile not handed over when a wait gave up
         if (KV) {
             // 64-query tile it: this warp's 32 columns [32*half, 32*half+32)
             // of S^T and dP^T in buffer it & 1; P^T and dS^T go to the first
@@ -495,7 +515,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                 ok = warp_wait(&bars.s_full[it & 1], (it >> 1) & 1u, bars.abort_flag, a.timeout_ns);
                 if (ok)  // the slot's statistics: this phase is complete and not yet refilled
                     ok = warp_wait(&bars.full_a[sa], (it / L::kSA) & 1u, bars.abort_flag, a.timeout_ns);
-                if (!ok) break;
+                if (!ok) {
+                    failed_at = it;
+                    break;
+                }
                 tc_fence_after();
                 const float* nlse2s = reinterpret_cast<const float*>(smem + L::kRingA + sa * L::kSlotA +
                                                                      2 * L::kTileIn);
@@ -543,13 +566,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.p_full[it & 1]);
+                named_barrier_arrive(kPBar + (it & 1), kEwThreads);
             }
         }
         for (int it = 0; !KV && it < tk.n && ok; ++it) {
             const int j = tk.j0 + it;
             ok = warp_wait(&bars.s_full[it & 1], (it >> 1) & 1u, bars.abort_flag, a.timeout_ns);
-            if (!ok) break;
+            if (!ok) {
+                failed_at = it;
+                break;
+            }
             tc_fence_after();
             const bool diag = CAUSAL && j == tk.blk;
             const uint32_t sb = t_s + 128u * static_cast<uint32_t>(it & 1) + lane_off + c0;
@@ -564,7 +590,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             reg_fence(sv);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.dp_free);
+            named_barrier_arrive(kDpBar, kEwThreads);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 if (c == 1) {
@@ -599,7 +625,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.p_full[it & 1]);
+            named_barrier_arrive(kPBar + (it & 1), kEwThreads);
+        }
+        if (!ok) {
+            // A wait gave up: hand over (nothing) for every tile not handed
+            // over yet, so that the issuing warp, which runs its schedule to
+            // the end, meets every named barrier it waits on.
+            for (int it = failed_at; it < tk.n; ++it) {
+                __syncwarp();
+                if (!KV) named_barrier_arrive(kDpBar, kEwThreads);
+                named_barrier_arrive(kPBar + (it & 1), kEwThreads);
+            }
         }
         // ---------------- epilogue: accumulators -> 16-bit rows ----------------
         // Each warp converts half of the D columns of its 32 rows.
