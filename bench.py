@@ -79,9 +79,9 @@ KERNEL_SOURCES = {"tc": ["fwd_tc.cu", "sm103_ptx.cuh"], "ffma": ["fwd_ffma.cu"],
                   "unfused": ["fwd_unfused.cu", "sm103_ptx.cuh"],
                   "bwd": ["bwd_tc.cu", "sm103_ptx.cuh"]}
 NCU_TRAFFIC = {
-    "bf16_B4_H16_N4096_D128": (201460736 + 35851008, "a321670f87af90f4"),
-    "bf16_B2_H32_N8192_D128_causal_qstd4": (2438488320 + 126081536, "a321670f87af90f4"),
-    "fp16_B1_H16_N16000_D64_causal": (127220480 + 13057280, "a321670f87af90f4"),
+    "bf16_B4_H16_N4096_D128": (202782208 + 37262592, "7a53c55660018186"),
+    "bf16_B2_H32_N8192_D128_causal_qstd4": (2186111232 + 120734464, "7a53c55660018186"),
+    "fp16_B1_H16_N16000_D64_causal": (153355264 + 14197504, "7a53c55660018186"),
     "fp32_B4_H8_N8192_D64_causal": (201679616 + 50925056, "e5b4a15b206c290b"),
 }
 
