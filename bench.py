@@ -13,8 +13,9 @@ std 4) the same way and adds it as the nested record `causal_target`
 Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
 events on the stream the kernel is launched on; L2 is flushed (a 512 MB
 buffer is rewritten) before every timed step, outside the events.  A short
-device-side spin before the first timed step lets the host queue the steps
-ahead of the GPU, so that no event pair includes host launch latency.  The whole
+device-side spin and two more untimed steps before the first timed step let
+the host queue the steps ahead of the GPU (no event pair includes host launch
+latency) and bring the clocks back up after the idle sampler start.  The whole
 timed loop is bracketed by a barrier and a device synchronise; the reported
 time is the max over ranks.  Under torchrun (N > 1) every rank runs the same
 workload on its own GPU (independent replicas: the method has no exchange
@@ -349,8 +350,13 @@ def run_ours(args, w, ws, rank, local):
     t0 = time.time()
     # A short device-side spin (outside every event pair) lets the host queue
     # the timed steps ahead of the GPU, so that no step's events include the
-    # host's launch latency.
+    # host's launch latency; two more untimed steps right before the timed
+    # ones bring the clocks back up after the idle time around the sampler
+    # start (the first step after an idle GPU ran about 10 % slower).
     torch.cuda._sleep(PRIME_CYCLES)
+    for _ in range(2):
+        flush.zero_()
+        step()
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
@@ -508,8 +514,13 @@ def run_ours_bwd(args, w, ws, rank, local):
     t0 = time.time()
     # A short device-side spin (outside every event pair) lets the host queue
     # the timed steps ahead of the GPU, so that no step's events include the
-    # host's launch latency.
+    # host's launch latency; two more untimed steps right before the timed
+    # ones bring the clocks back up after the idle time around the sampler
+    # start (the first step after an idle GPU ran about 10 % slower).
     torch.cuda._sleep(PRIME_CYCLES)
+    for _ in range(2):
+        flush.zero_()
+        step()
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
