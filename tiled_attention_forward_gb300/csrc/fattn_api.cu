@@ -169,6 +169,23 @@ cudaError_t host_pipe(HostPipe** out) {
     return cudaSuccess;
 }
 
+// Causal task order: query heads per group.  A group's K/V (16-bit) is
+// sized to stay in L2 while its tasks run (about 48 MB, so that the next
+// group's first tasks fit beside the last ones of this group), whole K/V
+// heads at a time (H / Hkv query heads share one), and the groups are made
+// as equal as the head count allows.
+int causal_head_group(int64_t BH, int64_t H, int64_t Hkv, int64_t N, int64_t D) {
+    constexpr int64_t kL2Budget = 48ll << 20;
+    const int64_t share = H / Hkv;
+    const int64_t kv_bytes = 2 * N * D * 2;
+    const int64_t kv_heads = std::max<int64_t>(1, kL2Budget / std::max<int64_t>(kv_bytes, 1));
+    const int64_t cap = std::min<int64_t>(BH, kv_heads * share);
+    const int64_t groups = ceil_div(BH, cap);
+    int64_t hg = ceil_div(BH, groups);
+    hg = ceil_div(hg, share) * share;  // whole K/V heads
+    return static_cast<int>(std::min<int64_t>(hg, BH));
+}
+
 }  // namespace
 
 cudaError_t tc_encode_maps(TcArgs& a, const void* q, const void* k, const void* v, int64_t BH,
@@ -332,6 +349,7 @@ int fattn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* l
     a.Hkv = static_cast<int>(Hkv);
     a.num_qblk = static_cast<int>(ceil_div(N, int64_t(kTcBM) * kTcQTiles));
     a.num_tasks = a.num_qblk * a.BH;
+    a.head_group = causal_head_group(BH, H, Hkv, N, D);
     a.scale_log2 = scale_log2;
     a.timeout_ns = kDefaultTimeoutNs;
     const int grid = static_cast<int>(std::min<int64_t>(a.num_tasks, sms));

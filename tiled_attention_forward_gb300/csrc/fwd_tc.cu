@@ -54,6 +54,16 @@ namespace fattn {
 // Bit k set <=> a kernel on this device hit fattn_status k (only TIMEOUT today).
 __device__ uint32_t g_error_word;
 
+// Task counters of the persistent grid.  CTAs take their first task by
+// index and every later one from a counter; a launch uses the slot its
+// %gridid (the context's launch number, new for every launch, graph replays
+// included) selects, so launches running at the same time use different
+// slots unless 65536 other grids were launched on the context in between,
+// and the last CTA to finish sets the slot back to zero.
+//   [0]: tasks handed out beyond the first gridDim.x; [1]: CTAs finished.
+constexpr uint32_t kSchedSlots = 1u << 16;
+__device__ uint32_t g_sched[kSchedSlots][2];
+
 namespace {
 
 constexpr uint32_t kSoftmaxRegs = 208;
@@ -78,9 +88,11 @@ struct TcLayout {
     // (P is handed to the MMA warp on named barriers, see kPBar.)
     static constexpr bool kRot = (D == 64);
     static constexpr int kSFull = kRot ? 6 : 2;
-    static constexpr int kNumBars = 2 + 2 + 2 * kStages + kSFull + 2 + (kRot ? 2 : 0) + 1;
-    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kBytes = kMiscOff + 16;
+    // ... then task_full[4] task_empty[4] (the ring of task indices)
+    static constexpr int kNumBars = 2 + 2 + 2 * kStages + kSFull + 2 + (kRot ? 2 : 0) + 1 + 8;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // TMEM base, abort flag
+    static constexpr int kTaskOff = kMiscOff + 16;            // uint64_t[kTaskRing]
+    static constexpr int kBytes = kTaskOff + 32;
     static constexpr int kAlloc = kBytes;  // the dynamic base is declared 1024-byte aligned
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kAlloc <= 227 * 1024, "shared memory budget");
@@ -98,16 +110,22 @@ struct Task {
 };
 
 // Task order: non-causal, head-major (all Q blocks of one head are adjacent so
-// concurrently running CTAs share that head's K/V in L2).  Causal, longest
-// first: Q blocks nearest the end of the sequence (most K/V tiles) are
-// scheduled first, heads inner; task_of() deals them out.
+// concurrently running CTAs share that head's K/V in L2).  Causal: heads in
+// groups of a.head_group (their K/V fits in L2 together), and within a group
+// longest first: Q blocks nearest the end of the sequence (most K/V tiles)
+// first, heads inner.  CTAs pull tasks in this order from a counter, so the
+// short tasks at the end of the last group fill in the tail.
 template <bool CAUSAL, bool EQUAL = false>
 __device__ __forceinline__ Task decode_task(int t, const TcArgs& a) {
     Task k;
     int qblk;
     if (CAUSAL) {
-        qblk = a.num_qblk - 1 - t / a.BH;
-        k.bh = t % a.BH;
+        const int per_group = a.head_group * a.num_qblk;
+        const int g = t / per_group;
+        const int r = t - g * per_group;
+        const int gsize = min(a.head_group, a.BH - g * a.head_group);
+        qblk = a.num_qblk - 1 - r / gsize;
+        k.bh = g * a.head_group + r % gsize;
     } else {
         qblk = t % a.num_qblk;
         k.bh = t / a.num_qblk;
@@ -137,15 +155,31 @@ __device__ __forceinline__ Task decode_task(int t, const TcArgs& a) {
     return k;
 }
 
-// The k-th task of this CTA.  Tasks are dealt in waves of gridDim.x, every
-// other wave in reverse CTA order (a snake), so that with the causal order
-// (longest first) each CTA's total work comes out nearly the same; a plain
-// stride gives CTA 0 the longest task of every wave.
-__device__ __forceinline__ int task_of(int k) {
-    const int g = static_cast<int>(gridDim.x);
-    const int c = (k & 1) ? g - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
-    return k * g + c;
+// The counter slot of this launch.
+__device__ __forceinline__ uint32_t* sched_slot() {
+    uint64_t id;
+    asm volatile("mov.u64 %0, %%gridid;" : "=l"(id));
+    return g_sched[id & (kSchedSlots - 1u)];
 }
+
+// The CTA's tasks go from the producer warp to the other roles through a
+// ring of kTaskRing shared-memory words (task_full / task_empty mbarriers).
+// Word kt % kTaskRing holds (kt << 32) | task once the CTA's kt-th task is
+// known; a task >= num_tasks ends the schedule.  Every role that meets
+// another on a named barrier must see the same sequence (named-barrier waits
+// are unbounded, see kPBar), also when a wait gives up: a reader whose wait
+// for word kt gave up writes "end" into it with a compare-and-swap, the
+// producer publishes with a compare-and-swap too, and whichever lands first
+// is what every reader of the word gets.
+constexpr int kTaskRing = 4;
+constexpr uint32_t kTaskReaders = 8 + 1;  // the softmax warps, the issuing warp
+constexpr uint32_t kEndOfSchedule = 0x7fffffffu;
+
+struct TaskRing {
+    uint64_t* full;            // [kTaskRing] mbarriers: word published
+    uint64_t* empty;           // [kTaskRing] mbarriers: word read by every reader
+    unsigned long long* word;  // [kTaskRing]
+};
 
 struct Bars {
     uint64_t* q_full;
@@ -156,6 +190,7 @@ struct Bars {
     uint64_t* o_full;
     uint64_t* o_ready;  // D = 64: [tile], one phase per completed P.V product
     uint64_t* drain;
+    TaskRing tasks;
 };
 
 template <int D>
@@ -171,6 +206,9 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
     r.o_full = r.s_full + L::kSFull;
     r.o_ready = r.o_full + 2;
     r.drain = r.o_ready + (L::kRot ? 2 : 0);
+    r.tasks.full = r.drain + 1;
+    r.tasks.empty = r.tasks.full + kTaskRing;
+    r.tasks.word = reinterpret_cast<unsigned long long*>(smem + L::kTaskOff);
     return r;
 }
 
@@ -190,6 +228,37 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
                                           volatile uint32_t* abort_flag, uint64_t timeout_ns) {
     return __all_sync(0xffffffffu,
                       mbar_wait_bounded(bar, parity, abort_flag, &g_error_word, timeout_ns));
+}
+
+__device__ __forceinline__ unsigned long long ring_word(int kt, uint32_t t) {
+    return (static_cast<unsigned long long>(static_cast<uint32_t>(kt)) << 32) | t;
+}
+__device__ __forceinline__ unsigned long long ring_peek(const TaskRing& r, int kt) {
+    return *reinterpret_cast<volatile unsigned long long*>(r.word + kt % kTaskRing);
+}
+
+// The CTA's kt-th task (whole warp; >= num_tasks: the schedule ended).
+__device__ __forceinline__ int read_task(const TaskRing& r, int kt, volatile uint32_t* abort_flag,
+                                         uint64_t timeout_ns) {
+    const int slot = kt % kTaskRing;
+    const bool arrived = warp_wait(&r.full[slot], (kt / kTaskRing) & 1, abort_flag, timeout_ns);
+    uint32_t t = 0u;
+    if ((threadIdx.x % 32) == 0) {
+        unsigned long long cur = ring_peek(r, kt);
+        if (!arrived && (cur >> 32) != static_cast<uint32_t>(kt)) {
+            const unsigned long long end = ring_word(kt, kEndOfSchedule);
+            const unsigned long long prev = atomicCAS(r.word + slot, cur, end);
+            cur = (prev == cur) ? end : prev;
+        }
+        t = static_cast<uint32_t>(cur);
+    }
+    return static_cast<int>(__shfl_sync(0xffffffffu, t, 0));
+}
+// A reader is done with word kt (the producer may reuse it for task kt + kTaskRing).
+__device__ __forceinline__ void release_task(const TaskRing& r, int kt) {
+    __syncwarp();
+    if ((threadIdx.x % 32) == 0) mbar_arrive(&r.empty[kt % kTaskRing]);
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -236,27 +305,45 @@ __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
         ++kv_it;
     };
 
+    uint32_t* ctr = sched_slot();
+    // Publish task t as the CTA's kt-th.  False: the wait for a free word
+    // gave up, or a reader has already ended the schedule there.
+    auto publish = [&](int kt, int t) -> bool {
+        const int slot = kt % kTaskRing;
+        if (kt >= kTaskRing &&
+            !warp_wait(&bars.tasks.empty[slot], ((kt / kTaskRing) - 1) & 1, abort_flag, a.timeout_ns))
+            return false;
+        uint32_t won = 0u;
+        if ((threadIdx.x % 32) == 0) {
+            const unsigned long long cur = ring_peek(bars.tasks, kt);
+            if ((cur >> 32) != static_cast<uint32_t>(kt)) {
+                won = atomicCAS(bars.tasks.word + slot, cur, ring_word(kt, static_cast<uint32_t>(t))) ==
+                      cur;
+                if (won) mbar_arrive(&bars.tasks.full[slot]);
+            }
+        }
+        return __shfl_sync(0xffffffffu, won, 0) != 0u;
+    };
+    // The next task from this launch's counter (the first gridDim.x tasks
+    // are the CTAs' own first ones).
+    auto fetch = [&]() -> int {
+        uint32_t v = 0u;
+        if ((threadIdx.x % 32) == 0) v = atomicAdd(&ctr[0], 1u);
+        v = __shfl_sync(0xffffffffu, v, 0);
+        return static_cast<int>(gridDim.x + min(v, static_cast<uint32_t>(a.num_tasks)));
+    };
+
+    int t = static_cast<int>(blockIdx.x);
     for (int kt = 0; ok; ++kt) {
-        const int t = task_of(kt);
-        if (t >= a.num_tasks) break;
+        if (t >= a.num_tasks) {
+            publish(kt, static_cast<int>(kEndOfSchedule));
+            break;
+        }
+        if (!publish(kt, t)) break;
         const Task tk = decode_task<CAUSAL, L::kRot>(t, a);
         const int kvh = kv_head_of(tk.bh, a.H, a.Hkv);
         load_q(0, tk);
         if (!ok) break;
-        // The next task's Q tiles are read once, from DRAM, and their loads
-        // can only start when this task's last score products are done;
-        // fetched into L2 now, they land in shared memory at L2 latency.
-        const int tn = task_of(kt + 1);
-        if (tn < a.num_tasks && elect_one_sync()) {
-            const Task nx = decode_task<CAUSAL, L::kRot>(tn, a);
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-                if (nx.q0 + i * kTcBM < a.N)
-#pragma unroll
-                    for (int at = 0; at < L::kAtoms; ++at)
-                        tma_prefetch_3d(&a.tmap_q, at * 64, nx.q0 + i * kTcBM, nx.bh);
-        }
-        __syncwarp();
         load_kv(&a.tmap_k, 0, kvh);
         if (!ok) break;
         if (tk.nb[1] > 0) {
@@ -267,6 +354,23 @@ __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
             load_kv(&a.tmap_v, j, kvh);
             if (ok && j + 1 < tk.nbmax) load_kv(&a.tmap_k, j + 1, kvh);
         }
+        if (!ok) break;
+        // The next task is taken only now, a few K/V tiles before this CTA
+        // runs out of work, so that the tasks still left go to the CTAs that
+        // become free first.  Its Q tiles are read once, from DRAM, and their
+        // loads can only start when this task's last score products are
+        // done; fetched into L2 now, they land in shared memory at L2 latency.
+        t = fetch();
+        if (t < a.num_tasks && elect_one_sync()) {
+            const Task nx = decode_task<CAUSAL, L::kRot>(t, a);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                if (nx.q0 + i * kTcBM < a.N)
+#pragma unroll
+                    for (int at = 0; at < L::kAtoms; ++at)
+                        tma_prefetch_3d(&a.tmap_q, at * 64, nx.q0 + i * kTcBM, nx.bh);
+        }
+        __syncwarp();
     }
 
     // Drain: every bulk copy this warp started has landed before the CTA can
@@ -346,6 +450,18 @@ __device__ void mma_pair_role(const TcArgs& a, uint8_t* smem, const Bars& bars, 
             tc_fence_after();
         }
     };
+    // The CTA's kt-th task: the helper waits for it, the issuing warp reads
+    // the same word after their meeting (also in a dry run).
+    auto next_task = [&](int kt) -> int {
+        int t = 0;
+        if (HELPER) t = read_task(bars.tasks, kt, abort_flag, a.timeout_ns);
+        sync();
+        if (!HELPER) {
+            t = static_cast<int>(static_cast<uint32_t>(ring_peek(bars.tasks, kt)));
+            release_task(bars.tasks, kt);
+        }
+        return t;
+    };
 
     // Descriptor templates with a zero start address.  A tile's descriptor is
     // the template plus (shared address >> 4): the start-address field is the
@@ -402,7 +518,7 @@ __device__ void mma_pair_role(const TcArgs& a, uint8_t* smem, const Bars& bars, 
     };
 
     for (int kt = 0;; ++kt) {
-        const int t = task_of(kt);
+        const int t = next_task(kt);
         if (t >= a.num_tasks) break;
         const Task tk = decode_task<CAUSAL>(t, a);
         uint32_t kslot, vslot;
@@ -529,6 +645,16 @@ __device__ void mma_pair_role_rot(const TcArgs& a, uint8_t* smem, const Bars& ba
             tc_fence_after();
         }
     };
+    auto next_task = [&](int kt) -> int {
+        int t = 0;
+        if (HELPER) t = read_task(bars.tasks, kt, abort_flag, a.timeout_ns);
+        sync();
+        if (!HELPER) {
+            t = static_cast<int>(static_cast<uint32_t>(ring_peek(bars.tasks, kt)));
+            release_task(bars.tasks, kt);
+        }
+        return t;
+    };
     const bool issuer = !HELPER;
     // S product into buffer b: Q tile i against the K tile in ring slot ks.
     auto issue_s = [&](uint32_t b, int i, uint32_t ks) {
@@ -551,7 +677,7 @@ __device__ void mma_pair_role_rot(const TcArgs& a, uint8_t* smem, const Bars& ba
     };
 
     for (int kt = 0;; ++kt) {
-        const int t = task_of(kt);
+        const int t = next_task(kt);
         if (t >= a.num_tasks) break;
         const Task tk = decode_task<CAUSAL, true>(t, a);
         const int nb = tk.nbmax;
@@ -627,16 +753,24 @@ __device__ void mma_pair_role_rot(const TcArgs& a, uint8_t* smem, const Bars& ba
 // Softmax + correction + epilogue (one warpgroup per Q tile), both layouts
 // ---------------------------------------------------------------------------
 // After a wait of a softmax warpgroup gave up: pass the P named barrier of
-// every block this tile has not handed over yet (block j0 of the CTA's kt0-th
-// task onwards), waiting on nothing, so that the issuing warp, which runs its
-// schedule to the end, meets every barrier it waits on (see kPBar).
+// every block this tile has not handed over yet -- blocks j0 .. nb0 - 1 of
+// the current task, then every block of the CTA's tasks from the kt1-th on
+// as the ring delivers them -- waiting on nothing else, so that the issuing
+// warp, which runs the same schedule to its end, meets every barrier it
+// waits on (see kPBar).
 template <bool CAUSAL, bool EQUAL>
-__device__ __noinline__ void softmax_dry_tail(const TcArgs& a, int tile, int kt0, int j0) {
-    for (int kt = kt0;; ++kt) {
-        const int t = task_of(kt);
+__device__ __noinline__ void softmax_dry_tail(const TcArgs& a, TaskRing tasks, int tile, int j0,
+                                              int nb0, int kt1, volatile uint32_t* abort_flag) {
+    for (int j = j0; j < nb0; ++j) {
+        __syncwarp();
+        named_barrier_arrive(p_bar(tile, j), kPBarThreads);
+    }
+    for (int kt = kt1;; ++kt) {
+        const int t = read_task(tasks, kt, abort_flag, a.timeout_ns);
         if (t >= a.num_tasks) break;
+        release_task(tasks, kt);
         const Task tk = decode_task<CAUSAL, EQUAL>(t, a);
-        for (int j = (kt == kt0) ? j0 : 0; j < tk.nb[tile]; ++j) {
+        for (int j = 0; j < tk.nb[tile]; ++j) {
             __syncwarp();
             named_barrier_arrive(p_bar(tile, j), kPBarThreads);
         }
@@ -661,8 +795,9 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
     uint32_t pv_base = 0;  // D = 64: P.V products of this tile in earlier tasks
     uint32_t sbase = 0;    // D = 64: S products of both tiles in earlier tasks
     for (int kt = 0;; ++kt) {
-        const int t = task_of(kt);
+        const int t = read_task(bars.tasks, kt, abort_flag, a.timeout_ns);
         if (t >= a.num_tasks) break;
+        release_task(bars.tasks, kt);
         const Task tk = decode_task<CAUSAL, kRot>(t, a);
         const int nb = tk.nb[tile];
         if constexpr (!kRot) {
@@ -692,7 +827,7 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
             const bool ok = warp_wait(&bars.s_full[kRot ? b * 2 + tile : b], use & 1u, abort_flag,
                                       a.timeout_ns);
             if (!ok) {
-                softmax_dry_tail<CAUSAL, kRot>(a, tile, kt, j);
+                softmax_dry_tail<CAUSAL, kRot>(a, bars.tasks, tile, j, nb, kt + 1, abort_flag);
                 return;
             }
             tc_fence_after();
@@ -748,7 +883,8 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
                         // (at D = 128 the commit of S_i(j) already implies it).
                         if (!warp_wait(&bars.o_ready[tile], (pv_base + j - 1) & 1u, abort_flag,
                                        a.timeout_ns)) {
-                            softmax_dry_tail<CAUSAL, kRot>(a, tile, kt, j);
+                            softmax_dry_tail<CAUSAL, kRot>(a, bars.tasks, tile, j, nb, kt + 1,
+                                                           abort_flag);
                             return;
                         }
                         tc_fence_after();
@@ -817,7 +953,7 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
         const bool ok = warp_wait(&bars.o_full[tile], ocnt & 1u, abort_flag, a.timeout_ns);
         ++ocnt;
         if (!ok) {
-            softmax_dry_tail<CAUSAL, kRot>(a, tile, kt + 1, 0);
+            softmax_dry_tail<CAUSAL, kRot>(a, bars.tasks, tile, 0, 0, kt + 1, abort_flag);
             return;
         }
         tc_fence_after();
@@ -884,6 +1020,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid
             mbar_init(&bars.kv_empty[s], 1);
         }
         mbar_init(bars.drain, 1);
+        for (int s = 0; s < kTaskRing; ++s) {
+            mbar_init(&bars.tasks.full[s], 1);
+            mbar_init(&bars.tasks.empty[s], kTaskReaders);
+            bars.tasks.word[s] = ring_word(-1, 0u);  // a tag no task index has
+        }
         *abort_flag = 0u;
         fence_barrier_init();
     }
@@ -928,6 +1069,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid
     if (warp == 8) {
         tc_fence_after();
         tmem_dealloc(tmem_base, L::kTmemCols);
+    }
+    if (threadIdx.x == 0) {
+        // The last CTA to finish puts the launch's counters back to zero
+        // (every other CTA has taken its last task before counting itself).
+        uint32_t* ctr = sched_slot();
+        __threadfence();
+        if (atomicAdd(&ctr[1], 1u) == gridDim.x - 1u) {
+            atomicExch(&ctr[0], 0u);
+            atomicExch(&ctr[1], 0u);
+        }
     }
 }
 

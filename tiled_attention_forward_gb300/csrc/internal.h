@@ -46,6 +46,7 @@ struct TcArgs {
     int Hkv;             // key/value heads per batch (H % Hkv == 0)
     int num_qblk;        // ceil(N / 256)
     int num_tasks;       // BH * num_qblk
+    int head_group;      // causal task order: query heads per group (K/V of a group stays in L2)
     float scale_log2;    // scale * log2(e)
     uint64_t timeout_ns; // bound of every barrier wait
 };
