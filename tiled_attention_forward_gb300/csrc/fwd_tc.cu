@@ -10,6 +10,8 @@
 //
 // One CTA per SM, persistent over tasks.  A task is one (batch*head, 256-row
 // Q block): two 128-row Q tiles that share every K/V tile the CTA streams.
+// CTAs take tasks from a per-launch counter as they run out of work
+// (causal problems: heads in L2-sized groups, longest Q blocks first).
 //
 // Warp roles (384 threads = three warpgroups):
 //   warps 0-3  softmax warpgroup 0: Q tile 0, thread t owns query row t
@@ -19,8 +21,9 @@
 //   warps 4-7  softmax warpgroup 1: same for Q tile 1
 //   warp 8     MMA issue (one elected lane): S_i = Q_i K_j^T (SS form),
 //              O_i += P_i V_j (TS form), tcgen05.commit -> mbarriers
-//   warp 9     TMA producer (one elected lane): Q tiles once per task, K/V tiles
-//              through a ring of shared-memory stages
+//   warp 9     TMA producer (one elected lane): takes the CTA's next task
+//              and publishes it to the other roles (task ring), Q tiles
+//              once per task, K/V tiles through a ring of shared-memory stages
 //   warp 10    the MMA warp's helper: does the MMA warp's barrier waits and
 //              releases it on a named barrier
 //   warp 11    idle
@@ -66,8 +69,8 @@ __device__ uint32_t g_sched[kSchedSlots][2];
 
 namespace {
 
-constexpr uint32_t kSoftmaxRegs = 208;
-constexpr uint32_t kControlRegs = 80;
+constexpr uint32_t kSoftmaxRegs = 216;
+constexpr uint32_t kControlRegs = 72;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kTcThreads * 168,
               "register split must fit the launch allocation");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 while the max is stale
@@ -88,11 +91,10 @@ struct TcLayout {
     // (P is handed to the MMA warp on named barriers, see kPBar.)
     static constexpr bool kRot = (D == 64);
     static constexpr int kSFull = kRot ? 6 : 2;
-    // ... then task_full[4] task_empty[4] (the ring of task indices)
-    static constexpr int kNumBars = 2 + 2 + 2 * kStages + kSFull + 2 + (kRot ? 2 : 0) + 1 + 8;
+    static constexpr int kNumBars = 2 + 2 + 2 * kStages + kSFull + 2 + (kRot ? 2 : 0) + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // TMEM base, abort flag
-    static constexpr int kTaskOff = kMiscOff + 16;            // uint64_t[kTaskRing]
-    static constexpr int kBytes = kTaskOff + 32;
+    static constexpr int kTaskOff = kMiscOff + 16;            // the task ring (TaskRing)
+    static constexpr int kBytes = kTaskOff + 3 * 4 * 8;
     static constexpr int kAlloc = kBytes;  // the dynamic base is declared 1024-byte aligned
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kAlloc <= 227 * 1024, "shared memory budget");
@@ -175,10 +177,20 @@ constexpr int kTaskRing = 4;
 constexpr uint32_t kTaskReaders = 8 + 1;  // the softmax warps, the issuing warp
 constexpr uint32_t kEndOfSchedule = 0x7fffffffu;
 
+// One shared-memory address locates the ring (a single register in the
+// softmax warps, which hold a whole score row): kTaskRing words, then their
+// "published" mbarriers, then their "read by every reader" mbarriers.
 struct TaskRing {
-    uint64_t* full;            // [kTaskRing] mbarriers: word published
-    uint64_t* empty;           // [kTaskRing] mbarriers: word read by every reader
-    unsigned long long* word;  // [kTaskRing]
+    uint32_t base;
+    __device__ __forceinline__ unsigned long long* word(int s) const {
+        return static_cast<unsigned long long*>(__cvta_shared_to_generic(base + 8u * s));
+    }
+    __device__ __forceinline__ uint64_t* full(int s) const {
+        return static_cast<uint64_t*>(__cvta_shared_to_generic(base + 8u * (kTaskRing + s)));
+    }
+    __device__ __forceinline__ uint64_t* empty(int s) const {
+        return static_cast<uint64_t*>(__cvta_shared_to_generic(base + 8u * (2 * kTaskRing + s)));
+    }
 };
 
 struct Bars {
@@ -206,9 +218,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
     r.o_full = r.s_full + L::kSFull;
     r.o_ready = r.o_full + 2;
     r.drain = r.o_ready + (L::kRot ? 2 : 0);
-    r.tasks.full = r.drain + 1;
-    r.tasks.empty = r.tasks.full + kTaskRing;
-    r.tasks.word = reinterpret_cast<unsigned long long*>(smem + L::kTaskOff);
+    r.tasks.base = smem_u32(smem + L::kTaskOff);
     return r;
 }
 
@@ -234,20 +244,20 @@ __device__ __forceinline__ unsigned long long ring_word(int kt, uint32_t t) {
     return (static_cast<unsigned long long>(static_cast<uint32_t>(kt)) << 32) | t;
 }
 __device__ __forceinline__ unsigned long long ring_peek(const TaskRing& r, int kt) {
-    return *reinterpret_cast<volatile unsigned long long*>(r.word + kt % kTaskRing);
+    return *reinterpret_cast<volatile unsigned long long*>(r.word(kt % kTaskRing));
 }
 
 // The CTA's kt-th task (whole warp; >= num_tasks: the schedule ended).
 __device__ __forceinline__ int read_task(const TaskRing& r, int kt, volatile uint32_t* abort_flag,
                                          uint64_t timeout_ns) {
     const int slot = kt % kTaskRing;
-    const bool arrived = warp_wait(&r.full[slot], (kt / kTaskRing) & 1, abort_flag, timeout_ns);
+    const bool arrived = warp_wait(r.full(slot), (kt / kTaskRing) & 1, abort_flag, timeout_ns);
     uint32_t t = 0u;
     if ((threadIdx.x % 32) == 0) {
         unsigned long long cur = ring_peek(r, kt);
         if (!arrived && (cur >> 32) != static_cast<uint32_t>(kt)) {
             const unsigned long long end = ring_word(kt, kEndOfSchedule);
-            const unsigned long long prev = atomicCAS(r.word + slot, cur, end);
+            const unsigned long long prev = atomicCAS(r.word(slot), cur, end);
             cur = (prev == cur) ? end : prev;
         }
         t = static_cast<uint32_t>(cur);
@@ -257,7 +267,7 @@ __device__ __forceinline__ int read_task(const TaskRing& r, int kt, volatile uin
 // A reader is done with word kt (the producer may reuse it for task kt + kTaskRing).
 __device__ __forceinline__ void release_task(const TaskRing& r, int kt) {
     __syncwarp();
-    if ((threadIdx.x % 32) == 0) mbar_arrive(&r.empty[kt % kTaskRing]);
+    if ((threadIdx.x % 32) == 0) mbar_arrive(r.empty(kt % kTaskRing));
     __syncwarp();
 }
 
@@ -311,15 +321,14 @@ __device__ void producer_role(const TcArgs& a, uint8_t* smem, const Bars& bars,
     auto publish = [&](int kt, int t) -> bool {
         const int slot = kt % kTaskRing;
         if (kt >= kTaskRing &&
-            !warp_wait(&bars.tasks.empty[slot], ((kt / kTaskRing) - 1) & 1, abort_flag, a.timeout_ns))
+            !warp_wait(bars.tasks.empty(slot), ((kt / kTaskRing) - 1) & 1, abort_flag, a.timeout_ns))
             return false;
         uint32_t won = 0u;
         if ((threadIdx.x % 32) == 0) {
             const unsigned long long cur = ring_peek(bars.tasks, kt);
             if ((cur >> 32) != static_cast<uint32_t>(kt)) {
-                won = atomicCAS(bars.tasks.word + slot, cur, ring_word(kt, static_cast<uint32_t>(t))) ==
-                      cur;
-                if (won) mbar_arrive(&bars.tasks.full[slot]);
+                won = atomicCAS(bars.tasks.word(slot), cur, ring_word(kt, static_cast<uint32_t>(t))) == cur;
+                if (won) mbar_arrive(bars.tasks.full(slot));
             }
         }
         return __shfl_sync(0xffffffffu, won, 0) != 0u;
@@ -1021,9 +1030,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_fwd_tc_kernel(const __grid
         }
         mbar_init(bars.drain, 1);
         for (int s = 0; s < kTaskRing; ++s) {
-            mbar_init(&bars.tasks.full[s], 1);
-            mbar_init(&bars.tasks.empty[s], kTaskReaders);
-            bars.tasks.word[s] = ring_word(-1, 0u);  // a tag no task index has
+            mbar_init(bars.tasks.full(s), 1);
+            mbar_init(bars.tasks.empty(s), kTaskReaders);
+            *bars.tasks.word(s) = ring_word(-1, 0u);  // a tag no task index has
         }
         *abort_flag = 0u;
         fence_barrier_init();
