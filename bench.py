@@ -82,9 +82,9 @@ KERNEL_SOURCES = {"tc": ["fwd_tc.cu", "sm103_ptx.cuh"], "ffma": ["fwd_ffma.cu"],
                   "unfused": ["fwd_unfused.cu", "sm103_ptx.cuh"],
                   "bwd": ["bwd_tc.cu", "sm103_ptx.cuh"]}
 NCU_TRAFFIC = {
-    "bf16_B4_H16_N4096_D128": (202782208 + 37262592, "7a53c55660018186"),
-    "bf16_B2_H32_N8192_D128_causal_qstd4": (2186111232 + 120734464, "7a53c55660018186"),
-    "fp16_B1_H16_N16000_D64_causal": (153355264 + 14197504, "7a53c55660018186"),
+    "bf16_B4_H16_N4096_D128": (201785344 + 38759936, "779f718b8db3dd8d"),
+    "bf16_B2_H32_N8192_D128_causal_qstd4": (411085312 + 112143872, "779f718b8db3dd8d"),
+    "fp16_B1_H16_N16000_D64_causal": (98410752 + 10502656, "779f718b8db3dd8d"),
     "fp32_B4_H8_N8192_D64_causal": (201679616 + 50925056, "e5b4a15b206c290b"),
 }
 
