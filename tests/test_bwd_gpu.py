@@ -80,6 +80,28 @@ def test_bwd_many_tiles_and_large_scores(causal):
                        dq_ref[b, h], dk_ref[b, h], dv_ref[b, h])
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("fp16", 64)])
+def test_bwd_many_heads(dtype, D, causal):
+    """192 heads of 257 rows: 576 CTAs per kernel, several waves of them on
+    the 152 SMs, checked on heads spread over the whole range."""
+    B, H, N = 4, 48, 257
+    q, k, v, do = make(B, H, N, D, DT[dtype], 500 + D)
+    scale = fattn._default_scale(D)
+    got = run_bwd(q, k, v, do, causal, scale)
+    q64, k64, v64, do64 = (to_f64(t) for t in (q, k, v, do))
+    dq_ref, dk_ref, dv_ref = oracle.backward(q64, k64, v64, do64, scale, causal)
+    o_ref, lse_ref = oracle.attention(q64, k64, v64, scale, causal)
+    allr = np.arange(N)
+    gots = tuple(to_f64(g) for g in got)
+    for bh in list(range(0, B * H, 13)) + [B * H - 1]:
+        b, h = divmod(bh, H)
+        check_head(q64[b, h], k64[b, h], v64[b, h], do64[b, h], o_ref[b, h], lse_ref[b, h],
+                   tuple(g[b, h] for g in gots), scale, causal, DT[dtype], allr, allr,
+                   "bwd B4 H48 N257 %s D%d causal=%s head %d" % (dtype, D, causal, bh),
+                   dq_ref[b, h], dk_ref[b, h], dv_ref[b, h])
+
+
 def test_bwd_is_deterministic():
     q, k, v, do = make(1, 3, 777, 64, torch.float16, 5)
     a = run_bwd(q, k, v, do, True, 0.125)
