@@ -817,8 +817,14 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
         const int lim = CAUSAL ? min(row + 1, a.N) : a.N;  // keys < lim are visible to this row
 
         float m_run = -INFINITY;  // running max of scale*log2(e)*s
-        float l_run = 0.f;        // running sum of the 16-bit P values fed to the MMA (normalises O)
-        float l_exact = 0.f;      // running sum of the unrounded P values (gives the LSE)
+        // bf16: O is normalised by the running sum of the 16-bit P values fed
+        // to the MMA, l_run, and the LSE comes from that of the unrounded
+        // values, l_exact.  fp16 rounds P 8x more finely, so one sum (of the
+        // unrounded values) serves both and the sum of the rounded ones is
+        // not formed.
+        constexpr bool kRoundedSum = BF16;
+        float l_run = 0.f;
+        float l_exact = 0.f;
 
         for (int j = 0; j < nb; ++j) {
             uint32_t b, use;
@@ -899,7 +905,7 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
                         tc_fence_after();
                     }
                     const float alpha = ex2_approx(m_run - m_new);
-                    l_run *= alpha;
+                    if constexpr (kRoundedSum) l_run *= alpha;
                     l_exact *= alpha;
                     m_run = m_new;
                     uint32_t r[32];
@@ -946,15 +952,17 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
             named_barrier_arrive(p_bar(tile, j), kPBarThreads);
             // The sum of the rounded P (which normalises O) feeds nothing the
             // MMA warp waits for, so it is formed after the hand-off.
-            float la[8];
+            if constexpr (kRoundedSum) {
+                float la[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) la[u] = 0.f;
+                for (int u = 0; u < 8; ++u) la[u] = 0.f;
 #pragma unroll
-            for (int c = 0; c < kTcBN / 32; ++c)
+                for (int c = 0; c < kTcBN / 32; ++c)
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    add_packed16_to_f32<BF16>(la[(e % 4) * 2], la[(e % 4) * 2 + 1], pk[c][e]);
-            l_run += ((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7]));
+                    for (int e = 0; e < 16; ++e)
+                        add_packed16_to_f32<BF16>(la[(e % 4) * 2], la[(e % 4) * 2 + 1], pk[c][e]);
+                l_run += ((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7]));
+            }
             l_exact += ((le[0] + le[1]) + (le[2] + le[3])) + ((le[4] + le[5]) + (le[6] + le[7]));
         }
 
@@ -966,7 +974,7 @@ __device__ void softmax_role(const TcArgs& a, const Bars& bars, uint32_t tmem_ba
             return;
         }
         tc_fence_after();
-        const float inv_l = 1.f / l_run;
+        const float inv_l = 1.f / (kRoundedSum ? l_run : l_exact);
         const bool valid = row < a.N;
         uint8_t* orow = reinterpret_cast<uint8_t*>(a.o) +
                         ((static_cast<int64_t>(tk.bh) * a.N + row) * D) * 2;
