@@ -13,12 +13,14 @@
 //          (-inf / 0 past N so that tail rows contribute nothing), negated so
 //          that the elementwise steps are plain packed adds and FMAs;
 //   dKdV : one CTA per (head, 128-key block): K and V stay in shared memory
-//          while 64-query tiles of Q, dO and their row statistics stream
-//          through a TMA ring; S^T = K Q^T and dP^T = V dO^T land in TMEM
-//          (two buffers), eight warps (one key row per thread, two warps per
-//          row range, 32 columns each) turn them into P^T and dS^T
-//          (16-bit, written back into TMEM), and dV += P^T dO, dK += dS^T Q
-//          accumulate in TMEM; dK and dV are written once at the end;
+//          while 128-query tiles of Q, dO and their row statistics stream
+//          through a TMA ring; S^T = K Q^T and dP^T = V dO^T land in TMEM,
+//          eight warps (one key row per thread, two warps per row range)
+//          turn them into P^T and dS^T (16-bit, written back into TMEM) one
+//          64-query half at a time, and dV += P^T dO, dK += dS^T Q
+//          accumulate in TMEM, the first half's products running while the
+//          warps work on the second, and the next tile's S^T while they
+//          finish; dK and dV are written once at the end;
 //   dQ   : one CTA per (head, 128-query tile), the mirror image: Q and dO
 //          stay, K and V stream, S = Q K^T and dP = dO V^T, dS formed per
 //          query row, dQ += dS K accumulates in TMEM.
@@ -45,30 +47,33 @@ constexpr int kMmaWarp = 8, kTmaWarp = 9, kHelperWarp = 10;
 // (a shared-memory access right after issued MMAs waits until they are
 // taken by the tensor pipe): the helper warp does those waits and meets it on
 // kSyncBar, with an AND of "every wait succeeded"; the elementwise warps hand
-// their 16-bit tiles (kPBar + tile parity: they can run one tile ahead) and,
-// for dQ, the dP columns they have read (kDpBar) over named barriers too.
+// their 16-bit tiles (dK/dV: kPBar + half of the 128-query tile; dQ: kPBar +
+// tile parity, since they can run one tile ahead) and, for dQ, the dP columns
+// they have read (kDpBar) over named barriers too.
 constexpr uint32_t kSyncBar = 1, kSyncThreads = 64;
 constexpr uint32_t kPBar = 2;        // 2, 3
 constexpr uint32_t kDpBar = 4;
+// dK/dV: the elementwise warps have loaded the last scores of a tile, so the
+// issuing warp may overwrite them with the next tile's.
+constexpr uint32_t kLdBar = 4;
 constexpr uint32_t kEwThreads = 8 * 32 + 32;  // the elementwise warps and the issuing warp
 constexpr uint32_t kTmemCols = 512;
 
 // Shared memory: the two resident tiles, then ring A and ring B.
-//   dK/dV: ring A slots hold a 64-query inner tile pair (Q, dO) and those
+//   dK/dV: ring A slots hold a 128-query inner tile pair (Q, dO) and those
 //          queries' LSE*log2e and Delta; ring B is empty (Q and dO are both
 //          read until the tile's accumulating products).
 //   dQ:    ring A holds K tiles, ring B V tiles: V is free once dP is done,
 //          earlier than K (read again by dQ += dS K), so the two rings are
 //          released separately and K gets the deeper one.
-constexpr int kBQ = 64;  // queries per inner tile of the dK/dV kernel
 
 template <int D, bool KV>
 struct BwdLayout {
     static constexpr int kTile = kBT * D * 2;               // one [128][D] 16-bit tile
-    static constexpr int kTileIn = KV ? kBQ * D * 2 : kTile; // one streamed inner tile
-    static constexpr int kAtomIn = KV ? kBQ * 128 : kBT * 128; // bytes of one 64-wide swizzle atom of it
-    static constexpr int kStats = KV ? 2 * kBQ * 4 : 0;     // LSE*log2e and Delta of the tile's queries
-    static constexpr int kSA = KV ? (D == 128 ? 4 : 6) : (D == 128 ? 3 : 4);
+    static constexpr int kTileIn = kTile;                   // one streamed inner tile (128 rows)
+    static constexpr int kAtomIn = kBT * 128;               // bytes of one 64-wide swizzle atom of it
+    static constexpr int kStats = KV ? 2 * kBT * 4 : 0;     // LSE*log2e and Delta of the tile's queries
+    static constexpr int kSA = KV ? (D == 128 ? 2 : 5) : (D == 128 ? 3 : 4);
     static constexpr int kSB = KV ? 0 : (D == 128 ? 2 : 4);
     static constexpr int kSBm = kSB > 0 ? kSB : 1;          // divisor for ring B indices
     static constexpr int kSlotA = KV ? (2 * kTileIn + kStats + 1023) / 1024 * 1024 : kTile;
@@ -78,8 +83,8 @@ struct BwdLayout {
     static constexpr int kRingB = kRingA + kSA * kSlotA;
     static constexpr int kBar = kRingB + kSB * kSlotB;
     // barriers: outer_full, fullA/emptyA[SA], fullB/emptyB[SB], s_full[2],
-    // done; abort flag; TMEM slot
-    static constexpr int kBytes = kBar + (4 + 2 * kSA + 2 * kSB) * 8 + 16;
+    // done, r_free; abort flag; TMEM slot
+    static constexpr int kBytes = kBar + (5 + 2 * kSA + 2 * kSB) * 8 + 16;
     static_assert(kBytes <= 227 * 1024, "shared memory");
 };
 
@@ -91,6 +96,7 @@ struct BwdBars {
     uint64_t* empty_b;
     uint64_t* s_full;
     uint64_t* done;
+    uint64_t* r_free;  // dK/dV at D = 64: a tile's second-half 16-bit results have been read
     uint32_t* abort_flag;
     uint32_t* tmem_slot;
 };
@@ -107,7 +113,8 @@ __device__ __forceinline__ BwdBars bwd_bars(uint8_t* smem) {
     b.empty_b = b.full_b + L::kSB;
     b.s_full = b.empty_b + L::kSB;   // [2]: one per S buffer / tile parity
     b.done = b.s_full + 2;
-    b.abort_flag = reinterpret_cast<uint32_t*>(b.done + 1);
+    b.r_free = b.done + 1;
+    b.abort_flag = reinterpret_cast<uint32_t*>(b.r_free + 1);
     b.tmem_slot = b.abort_flag + 1;
     return b;
 }
@@ -164,9 +171,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
 }
 
 // Work unit of a CTA.  dKdV: key block kb of key/value head bh (B*Hkv of
-// them); the inner tiles are the 64-query tiles j0 .. 2*nt-1 (causal: from the
-// first tile that meets the block's diagonal) of each of the H/Hkv query heads
-// that read this K/V head, head after head (n = group size x tiles per head).
+// them); the inner tiles are the 128-query tiles j0 .. nt-1 (causal: from the
+// tile on the block's diagonal) of each of the H/Hkv query heads that read
+// this K/V head, head after head (n = group size x tiles per head).
 // dQ: query tile qt of query head bh, key tiles 0 .. j_end-1 (causal: up to
 // the diagonal) of its K/V head.  Causal grids run the longest units first
 // (ascending kb, descending qt); otherwise head-major.
@@ -188,9 +195,9 @@ __device__ __forceinline__ BwdTask bwd_task(const BwdArgs& a) {
         t.bh = idx / a.num_tiles;
         t.blk = idx % a.num_tiles;
     }
-    if (KV) {  // 64-query inner tiles: two per 128-key block
-        t.j0 = CAUSAL ? 2 * t.blk : 0;
-        t.per_head = 2 * a.num_tiles - t.j0;
+    if (KV) {
+        t.j0 = CAUSAL ? t.blk : 0;
+        t.per_head = a.num_tiles - t.j0;
         t.n = t.per_head * (a.H / a.Hkv);
     } else {
         t.j0 = 0;
@@ -231,6 +238,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         }
         for (int i = 0; i < 2; ++i) mbar_init(&bars.s_full[i], 1);
         mbar_init(bars.done, 1);
+        mbar_init(bars.r_free, 1);
         *bars.abort_flag = 0u;
         fence_barrier_init();
     }
@@ -242,16 +250,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *bars.tmem_slot;
-    // TMEM columns.  dK/dV: two buffers b = tile parity, S^T_b [128b,128b+64)
-    // and dP^T_b [128b+64,128b+128) (64 queries each; the 16-bit P^T and dS^T
-    // overwrite S^T_b), dV [256,256+D), dK [256+D,256+2D).  dQ: S in two
-    // buffers [0,128) and [128,256) (then the 16-bit dS), dP [256,384),
-    // dQ [384,384+D).  Within a 32-column chunk of S the 16-bit results go to
-    // its first 16 columns (P, or dS for dQ) and, for dK/dV, dS^T to the next 16.
+    // TMEM columns.  dK/dV: S^T [0,128) and dP^T [128,256) of one 128-query
+    // tile; the 16-bit P^T and dS^T overwrite dP^T at D = 128 and have their
+    // own columns [256,384) at D = 64; then dV and dK (D columns each).  dQ: S in two buffers [0,128) and [128,256) (then
+    // the 16-bit dS), dP [256,384), dQ [384,384+D).  Within a 32-column chunk
+    // the 16-bit results go to its first 16 columns (P^T, or dS for dQ) and,
+    // for dK/dV, dS^T to the next 16.
     const uint32_t t_s = tmem;
-    const uint32_t t_dp = KV ? tmem + 64 : tmem + 256;   // dK/dV: + 128 * b
-    const uint32_t t_acc1 = KV ? tmem + 256 : tmem + 384;
-    const uint32_t t_acc2 = tmem + 256 + D;
+    const uint32_t t_dp = KV ? tmem + 128 : tmem + 256;
+    // dK/dV at D = 64: the 16-bit results in columns of their own, so the
+    // next tile's S^T and dP^T need not wait for the products that read them.
+    constexpr bool kOwnR = KV && D == 64;
+    const uint32_t t_r = kOwnR ? tmem + 256 : t_dp;
+    const uint32_t t_acc1 = KV ? tmem + (kOwnR ? 384 : 256) : tmem + 384;
+    const uint32_t t_acc2 = t_acc1 + D;
     const int blk0 = tk.blk * kBT;  // first row of the resident tiles
     // K/V head of the task (dK/dV: the task's own head; dQ: the one its query head reads)
     const int kvh = KV ? tk.bh : kv_head_of(tk.bh, a.H, a.Hkv);
@@ -261,8 +273,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         if (lane == 0) {
             const CUtensorMap* outer1 = KV ? &a.tmap_k : &a.tmap_q;
             const CUtensorMap* outer2 = KV ? &a.tmap_v : &a.tmap_do;
-            const CUtensorMap* inner1 = KV ? &a.tmap_q64 : &a.tmap_k;
-            const CUtensorMap* inner2 = KV ? &a.tmap_do64 : &a.tmap_v;
+            const CUtensorMap* inner1 = KV ? &a.tmap_q : &a.tmap_k;
+            const CUtensorMap* inner2 = KV ? &a.tmap_do : &a.tmap_v;
             mbar_arrive_expect_tx(bars.outer_full, 2 * L::kTile);
             const int oh = KV ? kvh : tk.bh;  // head of the resident tiles
             for (int at = 0; at < D / 64; ++at) {
@@ -273,7 +285,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             int issued_a = 0, issued_b = 0;
             bool ok = true;
             for (int it = 0; it < tk.n && ok; ++it) {
-                const int row0 = (tk.j0 + it % tk.per_head) * (KV ? kBQ : kBT);
+                const int row0 = (tk.j0 + it % tk.per_head) * kBT;
                 const int qh = KV ? bwd_query_head(a, tk, it) : tk.bh;  // head of the Q / dO tiles
                 const int sa = it % L::kSA;
                 if (it >= L::kSA) {
@@ -291,8 +303,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                 }
                 if (KV) {
                     const float* stats = a.ws + static_cast<int64_t>(qh) * 2 * a.Npad + row0;
-                    bulk_load(st + 2 * L::kTileIn, stats, kBQ * 4, &bars.full_a[sa]);
-                    bulk_load(st + 2 * L::kTileIn + kBQ * 4, stats + a.Npad, kBQ * 4, &bars.full_a[sa]);
+                    bulk_load(st + 2 * L::kTileIn, stats, kBT * 4, &bars.full_a[sa]);
+                    bulk_load(st + 2 * L::kTileIn + kBT * 4, stats + a.Npad, kBT * 4, &bars.full_a[sa]);
                 }
                 ++issued_a;
                 if (!KV) {
@@ -332,10 +344,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         }
     } else if (warp == kMmaWarp || warp == kHelperWarp) {
         // ---------------- MMA issue (warp 8) and its helper (warp 10) ----------------
-        // Both warps run the same schedule.  dK/dV: S^T and dP^T of 64-query
-        // tile it go to TMEM buffer it & 1; tiles it and it+1 are computed
-        // ahead, so while the elementwise warps work on one buffer the tensor
-        // pipe accumulates the previous tile and fills the other.  dQ: per
+        // Both warps run the same schedule.  dK/dV: S^T and dP^T of 128-query
+        // tile it (N = 128: the shared-memory operands at the tensor core's
+        // full rate, where N = 64 products run at two thirds of it) go to
+        // one TMEM buffer; the elementwise warps hand the 16-bit P^T and dS^T
+        // (written over dP^T) over one 64-query half at a time (kPBar +
+        // half), and the first half's accumulating products run while they
+        // work on the second.  S^T of tile it+1 is issued as soon as they
+        // have loaded the last scores of tile it (kLdBar), so it runs while
+        // they work too; dP^T of tile it+1 follows the second half's
+        // accumulating products, which read the columns it overwrites.  dQ: per
         // key tile it, S(it) and dP(it) -> s_full; the elementwise warps load
         // dP(it) and hand its columns back (kDpBar), so dP(it+1) (and
         // S(it+1), into the other buffer) run while they work, then dQ += dS K
@@ -344,9 +362,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         // barrier, which the elementwise warps then meet by arriving for
         // every remaining tile.
         const bool issuer = warp == kMmaWarp;
-        constexpr uint32_t kIdescS = idesc_f16_f32(kBT, KV ? kBQ : kBT, BF16 ? 1u : 0u, 0u, 0u);
+        constexpr uint32_t kIdescS = idesc_f16_f32(kBT, kBT, BF16 ? 1u : 0u, 0u, 0u);
         constexpr uint32_t kIdescAcc = idesc_f16_f32(kBT, D, BF16 ? 1u : 0u, 0u, 1u);
-        constexpr int kInRows = KV ? kBQ : kBT;
+        constexpr int kInRows = kBT;
         const uint64_t kmaj = smem_desc_sw128(0u, 16u, 1024u);
         const uint64_t mnmaj = smem_desc_sw128(0u, kInRows * 128u, 1024u);  // leading offset = slab size
         const uint32_t outer1_s = smem_u32(smem + L::kOuter), outer2_s = outer1_s + L::kTile;
@@ -354,8 +372,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         auto inner2 = [&](int it) {
             return KV ? inner1(it) + L::kTileIn : smem_u32(smem + L::kRingB + (it % L::kSBm) * L::kSlotB);
         };
-        auto s_buf = [&](int it) { return t_s + 128u * static_cast<uint32_t>(it & 1); };
-        auto dp_buf = [&](int it) { return KV ? s_buf(it) + 64u : t_dp; };
+        // dK/dV: one S^T / dP^T buffer; dQ: S in two buffers by tile parity.
+        auto s_buf = [&](int it) { return KV ? t_s : t_s + 128u * static_cast<uint32_t>(it & 1); };
+        auto dp_buf = [&](int it) { return t_dp; };
         // S = outer1 inner1^T, dP = outer2 inner2^T: both operands K-major over D.
         auto issue_s = [&](int it) {
 #pragma unroll
@@ -376,17 +395,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             }
         };
         // acc (+)= (16-bit tile in TMEM, 8 columns per 16 inner rows) x inner
-        // tile as an MN-major operand (16 inner rows = 2048 bytes).
-        auto issue_acc = [&](int it) {
+        // tile as an MN-major operand (16 inner rows = 2048 bytes), over the
+        // inner rows [64 h, 64 h + 64) (dQ: h = 0 and 1 in one go).  In each
+        // 32-column chunk (of dP^T for dK/dV, of S for dQ) the elementwise
+        // warp put its 16-bit results in the first 16 columns (P^T, or dS
+        // for dQ) and dS^T in the next 16.
+        auto issue_acc = [&](int it, int h, int halves) {
             const uint32_t in1 = inner1(it), in2 = inner2(it);
 #pragma unroll
-            for (int kk = 0; kk < kInRows / 16; ++kk) {
+            for (int kk = 4 * h; kk < 4 * (h + halves); ++kk) {
                 const uint64_t boff = (kk * 16 * 128) >> 4;
                 const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
                 const uint32_t acol = (kk / 2) * 32 + (kk % 2) * 8;
                 if (KV) {
-                    mma_ts(t_acc1, s_buf(it) + acol, mnmaj + (in2 >> 4) + boff, kIdescAcc, acc);       // dV += P^T dO
-                    mma_ts(t_acc2, s_buf(it) + acol + 16, mnmaj + (in1 >> 4) + boff, kIdescAcc, acc);  // dK += dS^T Q
+                    mma_ts(t_acc1, t_r + acol, mnmaj + (in2 >> 4) + boff, kIdescAcc, acc);       // dV += P^T dO
+                    mma_ts(t_acc2, t_r + acol + 16, mnmaj + (in1 >> 4) + boff, kIdescAcc, acc);  // dK += dS^T Q
                 } else {
                     mma_ts(t_acc1, s_buf(it) + acol, mnmaj + (in1 >> 4) + boff, kIdescAcc, acc);       // dQ += dS K
                 }
@@ -423,30 +446,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         };
         if (!issuer && ok) ok = warp_wait(bars.outer_full, 0u, bars.abort_flag, a.timeout_ns);
         if (KV) {
-            for (int t = 0; t < 2 && t < tk.n; ++t) {
-                wait_a(t);
-                sync();
-                issue([&] {
-                    issue_s(t);
-                    issue_dp(t);
-                    mma_commit(&bars.s_full[t]);
-                });
-            }
+            wait_a(0);
+            sync();
+            issue([&] {
+                issue_s(0);
+                issue_dp(0);
+                mma_commit(&bars.s_full[0]);
+            });
             for (int it = 0; it < tk.n; ++it) {
-                take(kPBar + (it & 1));
-                issue([&] {
-                    issue_acc(it);
-                    mma_commit(&bars.empty_a[it % L::kSA]);
-                });
-                if (it + 2 < tk.n) {  // tile it+2 into the buffer tile it has just released
-                    wait_a(it + 2);
+                const bool more = it + 1 < tk.n;
+                take(kPBar);
+                issue([&] { issue_acc(it, 0, 1); });
+                take(kLdBar);
+                if (more) {  // the next tile's scores over those just loaded
+                    wait_a(it + 1);
                     sync();
                     issue([&] {
-                        issue_s(it + 2);
-                        issue_dp(it + 2);
-                        mma_commit(&bars.s_full[it & 1]);
+                        issue_s(it + 1);
+                        if (kOwnR) {
+                            issue_dp(it + 1);
+                            mma_commit(&bars.s_full[0]);
+                        }
                     });
                 }
+                take(kPBar + 1);
+                issue([&] {
+                    issue_acc(it, 1, 1);
+                    mma_commit(&bars.empty_a[it % L::kSA]);
+                    if (kOwnR) mma_commit(bars.r_free);
+                    // D = 128: dP^T of tile it+1 in issue order after the
+                    // products that read tile it's 16-bit results from its columns.
+                    if (!kOwnR && more) {
+                        issue_dp(it + 1);
+                        mma_commit(&bars.s_full[0]);
+                    }
+                });
             }
         } else {
             wait_a(0);
@@ -477,7 +511,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                 }
                 take(kPBar + (it & 1));
                 issue([&] {
-                    issue_acc(it);
+                    issue_acc(it, 0, 2);
                     mma_commit(&bars.empty_a[it % L::kSA]);
                 });
             }
@@ -490,8 +524,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         // ---------------- elementwise warps 0-7 ----------------
         // Warps w and w+4 share TMEM lane quarter w % 4 (thread = lane =
         // resident row) and split the columns of S and dP between them (dK/dV:
-        // 32 each of a 64-query tile; dQ: 64 each of a 128-key tile); each
-        // writes its 16-bit results into the S columns it has already read.
+        // 32 each of each 64-query half of a 128-query tile; dQ: 64 each of a
+        // 128-key tile); each writes its 16-bit results into the S columns it
+        // has already read.
         const int quarter = warp % 4, half = warp / 4;
         const int r = quarter * 32 + lane;
         const int row = blk0 + r;  // KV: key index; dQ: query index
@@ -506,13 +541,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
         bool ok = true;
         int failed_at = 0;  // first tile not handed over when a wait gave up
         if (KV) {
-            // 64-query tile it: this warp's 32 columns [32*half, 32*half+32)
-            // of S^T and dP^T in buffer it & 1; P^T and dS^T go to the first
-            // 16 and the next 16 of those S^T columns.
+            // 128-query tile it, in two halves h: this warp's 32 columns
+            // [64h + 32*half, 64h + 32*half + 32) of S^T and dP^T; P^T and
+            // dS^T go to the first 16 and the next 16 of those dP^T columns,
+            // and each half is handed to the issuing warp on kPBar + h; once
+            // the second half's scores are in registers, S^T's columns are
+            // free (kLdBar).
             for (int it = 0; it < tk.n && ok; ++it) {
-                const int jq = tk.j0 + it % tk.per_head;  // 64-query tile index within its head
+                const int jq = tk.j0 + it % tk.per_head;  // 128-query tile index within its head
                 const int sa = it % L::kSA;
-                ok = warp_wait(&bars.s_full[it & 1], (it >> 1) & 1u, bars.abort_flag, a.timeout_ns);
+                ok = warp_wait(&bars.s_full[0], it & 1u, bars.abort_flag, a.timeout_ns);
                 if (ok)  // the slot's statistics: this phase is complete and not yet refilled
                     ok = warp_wait(&bars.full_a[sa], (it / L::kSA) & 1u, bars.abort_flag, a.timeout_ns);
                 if (!ok) {
@@ -522,51 +560,68 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
                 tc_fence_after();
                 const float* nlse2s = reinterpret_cast<const float*>(smem + L::kRingA + sa * L::kSlotA +
                                                                      2 * L::kTileIn);
-                const float* ndeltas = nlse2s + kBQ;
-                // queries before this key row exist only in the tiles that meet the block's diagonal
-                const bool diag = CAUSAL && jq < 2 * tk.blk + 2;
-                const int qoff = jq * kBQ - blk0;  // query - key = qoff + col - r
-                const uint32_t sb = t_s + 128u * static_cast<uint32_t>(it & 1) + lane_off + 32u * half;
-                uint32_t sv[32], dpv[32];
-                tmem_ld32(sb, sv);
-                tmem_ld32(sb + 64, dpv);
-                tmem_wait_ld();
-                reg_fence(sv);
-                reg_fence(dpv);
-                // P^T = exp2(s*scale*log2e - LSE2) and dS^T = P^T (dP^T - Delta),
-                // two queries per packed instruction; the statistics of the
-                // warp's 32 queries come as 16-byte broadcasts.
-                uint32_t pk[16], dsk[16];
-#pragma unroll
-                for (int e4 = 0; e4 < 32; e4 += 4) {
-                    const float4 nl = *reinterpret_cast<const float4*>(nlse2s + 32 * half + e4);
-                    const float4 nd = *reinterpret_cast<const float4*>(ndeltas + 32 * half + e4);
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int e = e4 + 2 * h2;
-                        const float nl0 = h2 ? nl.z : nl.x, nl1 = h2 ? nl.w : nl.y;
-                        const float nd0 = h2 ? nd.z : nd.x, nd1 = h2 ? nd.w : nd.y;
-                        float x0, x1, d0, d1;
-                        fma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), a.sl2, a.sl2,
-                             nl0, nl1);
-                        float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        if (diag) {  // queries before this key row are masked
-                            const int col = 32 * half + e;  // query jq*64 + col
-                            if (qoff + col < r) p0 = 0.f;
-                            if (qoff + col + 1 < r) p1 = 0.f;
-                        }
-                        add2(d0, d1, __uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1]), nd0, nd1);
-                        mul2(d0, d1, p0, p1, d0, d1);
-                        pk[e / 2] = pack16(p0, p1, BF16);
-                        dsk[e / 2] = pack16(d0, d1, BF16);
+                const float* ndeltas = nlse2s + kBT;
+                // queries before this key row exist only in the tile on the block's diagonal
+                const bool diag = CAUSAL && jq == tk.blk;
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    const int cq = 64 * h + 32 * half;  // this warp's first query column
+                    const uint32_t db = t_r + lane_off + cq;  // this warp's 16-bit results
+                    uint32_t sv[32], dpv[32];
+                    tmem_ld32(t_s + lane_off + cq, sv);
+                    tmem_ld32(t_dp + lane_off + cq, dpv);
+                    tmem_wait_ld();
+                    reg_fence(sv);
+                    reg_fence(dpv);
+                    if (h == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        named_barrier_arrive(kLdBar, kEwThreads);
                     }
+                    // P^T = exp2(s*scale*log2e - LSE2) and dS^T = P^T (dP^T - Delta),
+                    // two queries per packed instruction; the statistics of the
+                    // warp's 32 queries come as 16-byte broadcasts.
+                    uint32_t pk[16], dsk[16];
+#pragma unroll
+                    for (int e4 = 0; e4 < 32; e4 += 4) {
+                        const float4 nl = *reinterpret_cast<const float4*>(nlse2s + cq + e4);
+                        const float4 nd = *reinterpret_cast<const float4*>(ndeltas + cq + e4);
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int e = e4 + 2 * h2;
+                            const float nl0 = h2 ? nl.z : nl.x, nl1 = h2 ? nl.w : nl.y;
+                            const float nd0 = h2 ? nd.z : nd.x, nd1 = h2 ? nd.w : nd.y;
+                            float x0, x1, d0, d1;
+                            fma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), a.sl2, a.sl2,
+                                 nl0, nl1);
+                            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                            if (diag) {  // query cq + e of the tile against key r: hidden when before it
+                                if (cq + e < r) p0 = 0.f;
+                                if (cq + e + 1 < r) p1 = 0.f;
+                            }
+                            add2(d0, d1, __uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1]), nd0, nd1);
+                            mul2(d0, d1, p0, p1, d0, d1);
+                            pk[e / 2] = pack16(p0, p1, BF16);
+                            dsk[e / 2] = pack16(d0, d1, BF16);
+                        }
+                    }
+                    if (kOwnR && h == 1 && it > 0) {
+                        // The previous tile's second-half products read these
+                        // columns; they are issued after this tile's scores,
+                        // so only this half can get here before they are done.
+                        // (After a wait that gave up, the stores still go to
+                        // TMEM; nothing reads them any more.)
+                        ok = warp_wait(bars.r_free, (it - 1) & 1u, bars.abort_flag, a.timeout_ns);
+                        tc_fence_after();
+                    }
+                    tmem_st16(db, pk);
+                    tmem_st16(db + 16, dsk);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    named_barrier_arrive(kPBar + h, kEwThreads);
                 }
-                tmem_st16(sb, pk);
-                tmem_st16(sb + 16, dsk);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                named_barrier_arrive(kPBar + (it & 1), kEwThreads);
+                if (!ok) failed_at = it + 1;  // every barrier of this tile was met
             }
         }
         for (int it = 0; !KV && it < tk.n && ok; ++it) {
@@ -633,8 +688,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
             // the end, meets every named barrier it waits on.
             for (int it = failed_at; it < tk.n; ++it) {
                 __syncwarp();
-                if (!KV) named_barrier_arrive(kDpBar, kEwThreads);
-                named_barrier_arrive(kPBar + (it & 1), kEwThreads);
+                if (KV) {
+                    named_barrier_arrive(kPBar, kEwThreads);
+                    named_barrier_arrive(kLdBar, kEwThreads);
+                    named_barrier_arrive(kPBar + 1, kEwThreads);
+                } else {
+                    named_barrier_arrive(kDpBar, kEwThreads);
+                    named_barrier_arrive(kPBar + (it & 1), kEwThreads);
+                }
             }
         }
         // ---------------- epilogue: accumulators -> 16-bit rows ----------------

@@ -109,25 +109,6 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
-// 3-D map {D, N, heads} of a 16-bit [heads][N][D] tensor, box {64, rows, 1},
-// 128-byte swizzle, zero fill past N.
-cudaError_t encode_rows_map(CUtensorMap* map, const void* ptr, int64_t heads, int64_t N, int64_t D,
-                            uint32_t box_rows, bool bf16) {
-    auto encode = get_encode_fn();
-    if (!encode) return cudaErrorNotSupported;
-    const CUtensorMapDataType dt =
-        bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
-                                static_cast<cuuint64_t>(heads)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 2), static_cast<cuuint64_t>(N * D * 2)};
-    const cuuint32_t box[3] = {64, box_rows, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = encode(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 // Per-device helpers of fattn_fwd_host: a copy-in stream, a copy-out stream
 // and the events that chain them to the caller's stream, created on the first
 // call on the device and kept for the process lifetime.
@@ -564,9 +545,6 @@ int fattn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, co
     a.tmap_v = t.tmap_v;
     if (tc_encode_maps(t, dout, dout, dout, BH, BH, N, D, bf16) != cudaSuccess) return FATTN_ERR_CUDA;
     a.tmap_do = t.tmap_q;
-    if (encode_rows_map(&a.tmap_q64, q, BH, N, D, 64, bf16) != cudaSuccess ||
-        encode_rows_map(&a.tmap_do64, dout, BH, N, D, 64, bf16) != cudaSuccess)
-        return FATTN_ERR_CUDA;
     a.ws = static_cast<float*>(workspace);
     a.dq = dq;
     a.dk = dk;

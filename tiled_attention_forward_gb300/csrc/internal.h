@@ -109,8 +109,6 @@ struct BwdArgs {
     CUtensorMap tmap_k;
     CUtensorMap tmap_v;
     CUtensorMap tmap_do;
-    CUtensorMap tmap_q64; // Q and dO again with box {64, 64, 1}: the 64-query tiles of dK/dV
-    CUtensorMap tmap_do64;
     float* ws;            // [B*H][2][Npad]: LSE*log2(e) (+inf past N), Delta (0 past N)
     void* dq;             // [B,H,N,D] outputs, input dtype
     void* dk;
