@@ -82,9 +82,9 @@ KERNEL_SOURCES = {"tc": ["fwd_tc.cu", "sm103_ptx.cuh"], "ffma": ["fwd_ffma.cu"],
                   "unfused": ["fwd_unfused.cu", "sm103_ptx.cuh"],
                   "bwd": ["bwd_tc.cu", "sm103_ptx.cuh"]}
 NCU_TRAFFIC = {
-    "bf16_B4_H16_N4096_D128": (201829632 + 39738624, "bc872f40797ff7ea"),
-    "bf16_B2_H32_N8192_D128_causal_qstd4": (410912768 + 111794176, "bc872f40797ff7ea"),
-    "fp16_B1_H16_N16000_D64_causal": (98407936 + 10369024, "bc872f40797ff7ea"),
+    "bf16_B4_H16_N4096_D128": (201829632 + 39738624, "3a3002c616902885"),
+    "bf16_B2_H32_N8192_D128_causal_qstd4": (410912768 + 111794176, "3a3002c616902885"),
+    "fp16_B1_H16_N16000_D64_causal": (98407936 + 10369024, "3a3002c616902885"),
     "fp32_B4_H8_N8192_D64_causal": (201639936 + 51146240, "61c5185890f7842f"),
 }
 

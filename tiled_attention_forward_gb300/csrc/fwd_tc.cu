@@ -88,7 +88,8 @@ struct TcLayout {
     static constexpr int kBarOff = kKVOff + kStages * kKVTileBytes;
     // D = 128: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] o_full[2] drain[1]
     // D = 64 (three S buffers): ... s_full[3][2] o_full[2] o_ready[2] drain[1]
-    // (P is handed to the MMA warp on named barriers, see kPBar.)
+    // (P is handed to the MMA warp on named barriers, see kPBar; the task
+    // ring's words and barriers follow the misc words, see TaskRing.)
     static constexpr bool kRot = (D == 64);
     static constexpr int kSFull = kRot ? 6 : 2;
     static constexpr int kNumBars = 2 + 2 + 2 * kStages + kSFull + 2 + (kRot ? 2 : 0) + 1;
@@ -165,7 +166,8 @@ __device__ __forceinline__ uint32_t* sched_slot() {
 }
 
 // The CTA's tasks go from the producer warp to the other roles through a
-// ring of kTaskRing shared-memory words (task_full / task_empty mbarriers).
+// ring of kTaskRing shared-memory words, each with a "published" and a "read
+// by every reader" mbarrier.
 // Word kt % kTaskRing holds (kt << 32) | task once the CTA's kt-th task is
 // known; a task >= num_tasks ends the schedule.  Every role that meets
 // another on a named barrier must see the same sequence (named-barrier waits
