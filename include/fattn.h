@@ -314,6 +314,21 @@ FATTN_API int fattn_plan(int64_t B, int64_t H, int64_t N, int64_t D, int causal,
                int num_sms, int64_t out[9]);
 
 /*
+ * fattn_plan_head_group -- host only, no CUDA call: the number of query heads
+ * per group in fattn_fwd / fattn_fwd_gqa's causal task order.  The tensor-core
+ * kernel runs the causal tasks (256-row Q blocks) head group by head group,
+ * longest Q blocks first within a group, so that a group's K/V stays in L2;
+ * a group is made of whole K/V heads (H / Hkv query heads share one), holds
+ * about 48 MB of 16-bit K/V unless one K/V head is larger, and the groups are
+ * as equal as the head count allows.  Writes the group size (1 .. B*H) to
+ * *head_group.  Returns FATTN_ERR_INVALID_ARG for a null pointer, sizes < 1,
+ * D not in {64, 128} or H not a multiple of Hkv, FATTN_ERR_UNSUPPORTED past
+ * the kernels' index range, else FATTN_OK.
+ */
+FATTN_API int fattn_plan_head_group(int64_t B, int64_t H, int64_t Hkv, int64_t N, int64_t D,
+                                    int64_t* head_group);
+
+/*
  * fattn_get_device_status -- synchronises `stream`, then reads and clears the
  * current device's error word.  Returns FATTN_OK, FATTN_ERR_TIMEOUT if a
  * kernel gave up a bounded wait since the last call, FATTN_ERR_INTERNAL if a

@@ -300,3 +300,47 @@ def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(fattn, "_lib", None)
     with pytest.raises(fattn.FattnLibraryMissing):
         fattn.load()
+
+
+def test_plan_head_group_rules(lib):
+    """The causal task order's head groups: whole K/V heads, at most about
+    48 MB of 16-bit K/V per group unless a single K/V head is larger, and as
+    few groups as that budget allows, as equal in size as the heads allow."""
+    budget = 48 << 20
+    # hand-worked cases: 64 heads of 4 MiB K/V -> 12 fit, 6 groups of <= 11
+    assert fattn.plan_head_group(2, 32, 8192, 128) == 11
+    # 16 heads of 4.1 MB -> 11 fit, 2 groups of 8
+    assert fattn.plan_head_group(1, 16, 16000, 64) == 8
+    # 8 K/V heads of 8 MiB shared by pairs of query heads -> 6 K/V heads fit
+    assert fattn.plan_head_group(1, 16, 32768, 64, Hkv=8) == 8
+    # everything fits: one group
+    assert fattn.plan_head_group(1, 8, 1, 64) == 8
+    assert fattn.plan_head_group(3, 5, 1000, 128, Hkv=1) == 15
+    # one K/V head larger than the budget: groups of one K/V head
+    assert fattn.plan_head_group(1, 4, 1 << 20, 128) == 1
+    assert fattn.plan_head_group(1, 8, 1 << 20, 128, Hkv=2) == 4
+    for B, H, Hkv, N, D in [(1, 1, 1, 64, 64), (2, 7, 7, 8192, 128), (4, 16, 4, 16384, 128),
+                            (3, 24, 3, 30000, 64), (8, 32, 8, 4096, 128), (1, 40, 40, 12000, 64),
+                            (2, 12, 1, 65536, 128), (5, 9, 3, 20000, 128)]:
+        BH, share = B * H, H // Hkv
+        kv_head = 2 * N * D * 2
+        hg = fattn.plan_head_group(B, H, N, D, Hkv=Hkv)
+        assert 1 <= hg <= BH and hg % share == 0
+        assert (hg // share) * kv_head <= budget or hg == share
+        groups = -(-BH // hg)
+        # no fewer groups are possible within the budget
+        cap = max(share, (budget // kv_head) * share)
+        assert groups == -(-BH // min(BH, cap))
+        # the groups are as equal as whole K/V heads allow
+        last = BH - (groups - 1) * hg
+        assert 0 < last <= hg and hg - last < groups * share
+
+
+def test_plan_head_group_rejects(lib):
+    import ctypes
+    out = ctypes.c_int64(7)
+    assert lib.fattn_plan_head_group(1, 6, 4, 128, 64, ctypes.byref(out)) == 1
+    assert lib.fattn_plan_head_group(1, 4, 4, 128, 96, ctypes.byref(out)) == 1
+    assert lib.fattn_plan_head_group(0, 4, 4, 128, 64, ctypes.byref(out)) == 1
+    assert lib.fattn_plan_head_group(1, 4, 4, 128, 64, None) == 1
+    assert lib.fattn_plan_head_group(1, 4, 4, (1 << 30) + 1, 64, ctypes.byref(out)) == 2

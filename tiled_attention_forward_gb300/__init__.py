@@ -81,13 +81,15 @@ def load():
     lib.fattn_unfused_workspace_bytes.argtypes = [i64, i64, i64]
     lib.fattn_unfused_workspace_bytes.restype = i64
     lib.fattn_plan.argtypes = [i64, i64, i64, i64, ci, ci, ci, ctypes.POINTER(i64)]
+    lib.fattn_plan_head_group.argtypes = [i64, i64, i64, i64, i64, ctypes.POINTER(i64)]
     lib.fattn_get_device_status.argtypes = [vp]
     lib.fattn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.fattn_status_string.argtypes = [ci]
     lib.fattn_status_string.restype = ctypes.c_char_p
     lib.fattn_version.argtypes = []
     for f in ("fattn_fwd", "fattn_fwd_gqa", "fattn_fwd_host", "fattn_fwd_unfused", "fattn_bwd", "fattn_bwd_gqa", "fattn_bwd_host",
-              "fattn_fwd_unfused_static", "fattn_plan", "fattn_get_device_status",
+              "fattn_fwd_unfused_static", "fattn_plan", "fattn_plan_head_group",
+              "fattn_get_device_status",
               "fattn_selftest_wait_timeout", "fattn_version"):
         getattr(lib, f).restype = ci
     _lib = lib
@@ -355,6 +357,15 @@ def plan(B, H, N, D, causal=False, dtype=torch.bfloat16, num_sms=0):
     rc = load().fattn_plan(B, H, N, D, int(bool(causal)), code, int(num_sms), out)
     _check(rc, "fattn_plan")
     return dict(zip(PLAN_FIELDS, list(out)))
+
+
+def plan_head_group(B, H, N, D, Hkv=None):
+    """Query heads per group of the causal task order (host only); see
+    fattn_plan_head_group."""
+    out = ctypes.c_int64(0)
+    rc = load().fattn_plan_head_group(B, H, H if Hkv is None else Hkv, N, D, ctypes.byref(out))
+    _check(rc, "fattn_plan_head_group")
+    return out.value
 
 
 def get_device_status(stream=None):

@@ -234,6 +234,19 @@ const char* fattn_status_string(int status) {
     }
 }
 
+int fattn_plan_head_group(int64_t B, int64_t H, int64_t Hkv, int64_t N, int64_t D,
+                          int64_t* head_group) {
+    if (!head_group) return FATTN_ERR_INVALID_ARG;
+    *head_group = 0;
+    if (B < 1 || H < 1 || Hkv < 1 || N < 1 || (D != 64 && D != 128) || H % Hkv != 0)
+        return FATTN_ERR_INVALID_ARG;
+    if (N > (int64_t(1) << 30) || B > (int64_t(1) << 30) || H > (int64_t(1) << 30) ||
+        B * H > (int64_t(1) << 30))
+        return FATTN_ERR_UNSUPPORTED;
+    *head_group = causal_head_group(B * H, H, Hkv, N, D);
+    return FATTN_OK;
+}
+
 int fattn_plan(int64_t B, int64_t H, int64_t N, int64_t D, int causal, int dtype, int num_sms,
                int64_t out[9]) {
     if (!out) return FATTN_ERR_INVALID_ARG;
