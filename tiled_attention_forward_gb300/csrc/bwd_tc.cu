@@ -738,46 +738,78 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kernel(const __grid_c
 }
 
 // -LSE_i * log2(e) and -Delta_i, Delta_i = dO_i . O_i (fp32 over the 16-bit
-// inputs), one warp per row of the padded workspace [B*H][2][Npad]; rows
-// past N get -inf and 0.
+// inputs), into the padded workspace [B*H][2][Npad]; rows past N get -inf
+// and 0.  A row is read as 16-byte pieces by D/8 lanes, a warp covers
+// 32/(D/8) rows per load and keeps kPrepLoads such loads of O and of dO in
+// flight (kPrepRows rows per warp), so the kernel streams at memory rate.
+constexpr int kPrepLoads = 4;
+template <int D>
+__host__ __device__ constexpr int prep_rows_per_warp() { return (32 / (D / 8)) * kPrepLoads; }
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const void* __restrict__ o,
                                                             const void* __restrict__ dout,
                                                             const float* __restrict__ lse,
                                                             float* __restrict__ ws, int N, int Npad,
                                                             int64_t rows_padded) {
+    constexpr int kLanesPerRow = D / 8;               // 16-byte pieces per row
+    constexpr int kRowsPerLoad = 32 / kLanesPerRow;
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
     const int lane = threadIdx.x % 32;
-    if (gw >= rows_padded) return;
-    const int64_t bh = gw / Npad;
-    const int i = static_cast<int>(gw % Npad);
-    float nlse2 = -INFINITY, ndelta = 0.f;
-    if (i < N) {
-        const int64_t row = bh * N + i;
-        constexpr int kPer = D / 32;  // 16-bit elements per lane: 2 or 4
-        const uint16_t* orow = reinterpret_cast<const uint16_t*>(o) + row * D + lane * kPer;
-        const uint16_t* drow = reinterpret_cast<const uint16_t*>(dout) + row * D + lane * kPer;
+    const int sub = lane / kLanesPerRow, piece = lane % kLanesPerRow;
+    uint4 ov[kPrepLoads], dv[kPrepLoads];
+    int64_t prow[kPrepLoads];
+#pragma unroll
+    for (int k = 0; k < kPrepLoads; ++k) {
+        prow[k] = gw * prep_rows_per_warp<D>() + k * kRowsPerLoad + sub;  // padded row
+        ov[k] = make_uint4(0u, 0u, 0u, 0u);
+        dv[k] = ov[k];
+        if (prow[k] < rows_padded) {
+            const int64_t bh = prow[k] / Npad;
+            const int i = static_cast<int>(prow[k] % Npad);
+            if (i < N) {
+                const int64_t off = ((bh * N + i) * D) * 2 + piece * 16;
+                ov[k] = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(o) + off);
+                dv[k] = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(dout) + off);
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kPrepLoads; ++k) {
+        const uint32_t ow[4] = {ov[k].x, ov[k].y, ov[k].z, ov[k].w};
+        const uint32_t dw[4] = {dv[k].x, dv[k].y, dv[k].z, dv[k].w};
         float acc = 0.f;
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) {
-            float x, y;
+        for (int w = 0; w < 4; ++w) {
+            float x0, x1, y0, y1;
             if (BF16) {
-                x = __bfloat162float(__ushort_as_bfloat16(orow[e]));
-                y = __bfloat162float(__ushort_as_bfloat16(drow[e]));
+                const __nv_bfloat162 xb = *reinterpret_cast<const __nv_bfloat162*>(&ow[w]);
+                const __nv_bfloat162 yb = *reinterpret_cast<const __nv_bfloat162*>(&dw[w]);
+                x0 = __low2float(xb); x1 = __high2float(xb);
+                y0 = __low2float(yb); y1 = __high2float(yb);
             } else {
-                x = __half2float(__ushort_as_half(orow[e]));
-                y = __half2float(__ushort_as_half(drow[e]));
+                const __half2 xh = *reinterpret_cast<const __half2*>(&ow[w]);
+                const __half2 yh = *reinterpret_cast<const __half2*>(&dw[w]);
+                x0 = __low2float(xh); x1 = __high2float(xh);
+                y0 = __low2float(yh); y1 = __high2float(yh);
             }
-            acc = fmaf(x, y, acc);
+            acc = fmaf(x0, y0, acc);
+            acc = fmaf(x1, y1, acc);
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        ndelta = -acc;
-        nlse2 = -lse[row] * 1.4426950408889634f;
-    }
-    if (lane == 0) {
-        ws[bh * 2 * Npad + i] = nlse2;
-        ws[(bh * 2 + 1) * Npad + i] = ndelta;
+        for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, off, kLanesPerRow);
+        if (piece == 0 && prow[k] < rows_padded) {
+            const int64_t bh = prow[k] / Npad;
+            const int i = static_cast<int>(prow[k] % Npad);
+            float nlse2 = -INFINITY, ndelta = 0.f;
+            if (i < N) {
+                ndelta = -acc;
+                nlse2 = -lse[bh * N + i] * 1.4426950408889634f;
+            }
+            ws[bh * 2 * Npad + i] = nlse2;
+            ws[(bh * 2 + 1) * Npad + i] = ndelta;
+        }
     }
 }
 
@@ -785,7 +817,8 @@ template <int D, bool BF16, bool CAUSAL>
 cudaError_t bwd_launch_all(const BwdArgs& a, const void* o, const void* dout, const float* lse,
                            cudaStream_t stream) {
     const int64_t rows_padded = static_cast<int64_t>(a.BH) * a.Npad;
-    attn_bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((rows_padded + 7) / 8), 256, 0, stream>>>(
+    const int64_t prep_warps = (rows_padded + prep_rows_per_warp<D>() - 1) / prep_rows_per_warp<D>();
+    attn_bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((prep_warps + 7) / 8), 256, 0, stream>>>(
         o, dout, lse, a.ws, a.N, a.Npad, rows_padded);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
