@@ -99,9 +99,9 @@ NCU_TRAFFIC_UNFUSED = {
 
 # The backward: DRAM bytes of one step (statistics, dK/dV and dQ kernels).
 NCU_TRAFFIC_BWD = {
-    "bf16_B4_H16_N4096_D128": (676878336 + 154278400, "d3d5cd4fbd35f9e5"),
-    "bf16_B2_H32_N8192_D128_causal_qstd4": (7983200000 + 355654144, "d3d5cd4fbd35f9e5"),
-    "fp16_B1_H16_N16000_D64_causal": (465529088 + 51159296, "d3d5cd4fbd35f9e5"),
+    "bf16_B4_H16_N4096_D128": (676513536 + 154105856, "77268889cef676d6"),
+    "bf16_B2_H32_N8192_D128_causal_qstd4": (7977567744 + 355400704, "77268889cef676d6"),
+    "fp16_B1_H16_N16000_D64_causal": (463855360 + 51330816, "77268889cef676d6"),
 }
 
 
