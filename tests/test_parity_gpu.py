@@ -53,10 +53,12 @@ def test_tensor_core_many_tasks(dtype, D, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_tensor_core_large_scores(causal):
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_tensor_core_large_scores(dtype, causal):
     """Q ~ N(0, 16): scores of std 4 make the running max move by large steps,
-    exercising the (conditional) O rescale."""
-    run_case(1, 4, 700, 128, "bf16", causal, seed=400, q_std=4.0)
+    exercising the (conditional) O rescale; fp16 also exercises O normalised
+    by the sum of the unrounded P while the largest P of a row can exceed 1."""
+    run_case(1, 4, 700, 128, dtype, causal, seed=400, q_std=4.0)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
